@@ -1,0 +1,248 @@
+"""GB300 (sm_103a) block-scaled fused MoE layer: Python binding.
+
+Argument marshalling only: every function forwards to the entry point of the
+same name in ``libmoe_mx.so`` (declared in ``include/moe_mx.h``); all work
+runs in that library's CUDA kernels. PyTorch supplies device memory and the
+current stream. There is no fallback: if the library is missing, or a tensor
+is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "lib", "MoeError", "moe_sort", "moe_sort_max_padded", "moe_quant_act_mx",
+    "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
+    "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
+]
+
+HEADER = os.path.join(_build.ROOT, "include", "moe_mx.h")
+
+_c_void_p = ctypes.c_void_p
+_c_int = ctypes.c_int
+_c_size_t = ctypes.c_size_t
+_c_int64 = ctypes.c_int64
+
+
+class MoeWsLayout(ctypes.Structure):
+    _fields_ = [("block_m", ctypes.c_int32), ("_pad", ctypes.c_int32), ("p_max", _c_int64),
+                ("status_off", _c_int64), ("expert_off_off", _c_int64),
+                ("sorted_route_off", _c_int64), ("sorted_w_off", _c_int64),
+                ("block_expert_off", _c_int64), ("route_pos_off", _c_int64),
+                ("act_off", _c_int64), ("act_sf_off", _c_int64), ("inter_off", _c_int64),
+                ("inter_sf_off", _c_int64), ("acc_off", _c_int64), ("total_bytes", _c_int64)]
+
+
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [_c_int]),
+    "moe_sort_max_padded": (_c_int64, [_c_int, _c_int, _c_int, _c_int]),
+    "moe_sort": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p,
+                          _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "moe_quant_act_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_void_p,
+                                  _c_void_p]),
+    "moe_prepacked_scale_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
+    "moe_prepack_scales_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_void_p]),
+    "fused_moe_workspace_bytes": (_c_size_t, [_c_int] * 6),
+    "fused_moe_workspace_layout": (_c_int, [_c_int] * 6 + [ctypes.POINTER(MoeWsLayout)]),
+    "fused_moe_a8w4": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
+                                _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
+    "fused_moe_a16w4": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                 _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
+                                 _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
+    "moe_decode_device_status": (_c_int, [ctypes.c_int32]),
+}
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(
+                f"{_build.LIB} is missing: build it with __graft_entry__.build() or "
+                "`python -m block_scaled_moe_sort_gb300.build`")
+        L = ctypes.CDLL(_build.LIB)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def declared_functions() -> list:
+    """Names of the functions include/moe_mx.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = lib().moe_status_string(code).decode()
+        super().__init__(f"{fn}: {msg} (status {code})")
+        self.code = code
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise MoeError(fn, code)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# ----------------------------------------------------------------- sort
+
+def moe_sort_max_padded(M: int, topk: int, E: int, block_m: int) -> int:
+    return int(lib().moe_sort_max_padded(M, topk, E, block_m))
+
+
+def moe_sort(topk_ids: torch.Tensor, topk_weights: torch.Tensor, E: int, block_m: int,
+             stream=None) -> dict:
+    """Sorted route lists of ``topk_ids`` [M, topk] (see moe_mx.h)."""
+    M, topk = topk_ids.shape
+    assert topk_ids.dtype == torch.int32 and topk_weights.dtype == torch.float32
+    pm = moe_sort_max_padded(M, topk, E, block_m)
+    if pm < 0:
+        raise ValueError("unsupported sort shape")
+    dev = topk_ids.device
+    out = dict(
+        sorted_route=torch.empty(pm, dtype=torch.int32, device=dev),
+        sorted_w=torch.empty(pm, dtype=torch.float32, device=dev),
+        block_expert=torch.empty(pm // block_m, dtype=torch.int32, device=dev),
+        expert_off=torch.empty(E + 1, dtype=torch.int32, device=dev),
+        num_padded=torch.empty(1, dtype=torch.int32, device=dev),
+        route_pos=torch.empty(M * topk, dtype=torch.int32, device=dev),
+    )
+    code = lib().moe_sort(_ptr(topk_ids), _ptr(topk_weights), M, topk, E, block_m,
+                          out["sorted_route"].data_ptr(), out["sorted_w"].data_ptr(),
+                          out["block_expert"].data_ptr() if pm else None,
+                          out["expert_off"].data_ptr(), out["num_padded"].data_ptr(),
+                          _ptr(out["route_pos"]), _stream(stream))
+    _check("moe_sort", code)
+    return out
+
+
+# ---------------------------------------------------------------- quant
+
+def moe_quant_act_mx(x: torch.Tensor, stream=None):
+    """BF16 [M, K] -> (E4M3 codes uint8 [M, K], E8M0 scales uint8 [M, K/32])."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2
+    M, K = x.shape
+    q = torch.empty(M, K, dtype=torch.uint8, device=x.device)
+    s = torch.empty(M, K // 32, dtype=torch.uint8, device=x.device)
+    _check("moe_quant_act_mx", lib().moe_quant_act_mx(_ptr(x), M, K, K, _ptr(q), _ptr(s),
+                                                      _stream(stream)))
+    return q, s
+
+
+def moe_prepack_scales_mx(scale: torch.Tensor, stream=None) -> torch.Tensor:
+    """Row-major E8M0 weight scales [E, N, K/32] -> MMA scale atoms."""
+    assert scale.dtype == torch.uint8 and scale.dim() == 3
+    E, N, KB = scale.shape
+    K = KB * 32
+    nbytes = int(lib().moe_prepacked_scale_bytes(E, N, K))
+    if nbytes == 0:
+        raise ValueError("unsupported scale shape (N and K must be multiples of 128)")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=scale.device)
+    _check("moe_prepack_scales_mx", lib().moe_prepack_scales_mx(_ptr(scale), E, N, K, _ptr(out),
+                                                                _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------- fused layer
+
+def fused_moe_workspace_bytes(M: int, H: int, Ip: int, E: int, topk: int, a16: bool) -> int:
+    return int(lib().fused_moe_workspace_bytes(M, H, Ip, E, topk, int(a16)))
+
+
+def fused_moe_workspace_layout(M: int, H: int, Ip: int, E: int, topk: int, a16: bool) -> dict:
+    L = MoeWsLayout()
+    _check("fused_moe_workspace_layout",
+           lib().fused_moe_workspace_layout(M, H, Ip, E, topk, int(a16), ctypes.byref(L)))
+    return {f: getattr(L, f) for f, _ in MoeWsLayout._fields_ if f != "_pad"}
+
+
+def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
+           out=None, ws=None, stream=None):
+    M, H = x.shape
+    topk = topk_ids.shape[1]
+    E = w1.shape[0]
+    Ip = w2.shape[2] * 2
+    a16 = fn_name == "fused_moe_a16w4"
+    assert x.dtype == torch.bfloat16 and topk_ids.dtype == torch.int32
+    assert topk_weights.dtype == torch.float32 and w1.dtype == torch.uint8
+    assert w1.shape == (E, 2 * Ip, H // 2) and w2.shape == (E, H, Ip // 2)
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(fused_moe_workspace_bytes(M, H, Ip, E, topk, a16), 1),
+                         dtype=torch.uint8, device=x.device)
+    code = getattr(lib(), fn_name)(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, H, topk, _ptr(w1),
+        _ptr(w1_scale_packed), _ptr(w2), _ptr(w2_scale_packed), E, Ip, _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream))
+    _check(fn_name, code)
+    return out
+
+
+def fused_moe_a8w4(x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
+                   out=None, ws=None, stream=None) -> torch.Tensor:
+    """FP8-activation x MXFP4-weight fused MoE; returns BF16 [M, H]."""
+    return _fused("fused_moe_a8w4", x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
+                  w2_scale_packed, out, ws, stream)
+
+
+def fused_moe_a16w4(x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
+                    out=None, ws=None, stream=None) -> torch.Tensor:
+    """BF16-activation x MXFP4-weight fused MoE; returns BF16 [M, H]."""
+    return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
+                  w2_scale_packed, out, ws, stream)
+
+
+class MoeLayer:
+    """Device-resident MXFP4 expert weights with prepacked scales."""
+
+    def __init__(self, w1, w1_scale, w2, w2_scale, a16: bool = False, device="cuda"):
+        self.a16 = a16
+        self.w1 = w1.to(device).contiguous()
+        self.w2 = w2.to(device).contiguous()
+        self.w1_scale = moe_prepack_scales_mx(w1_scale.to(device).contiguous())
+        self.w2_scale = moe_prepack_scales_mx(w2_scale.to(device).contiguous())
+        self.E = self.w1.shape[0]
+        self.H = self.w2.shape[1]
+        self.Ip = self.w2.shape[2] * 2
+
+    def workspace_bytes(self, M: int, topk: int) -> int:
+        return fused_moe_workspace_bytes(M, self.H, self.Ip, self.E, topk, self.a16)
+
+    def __call__(self, x, topk_ids, topk_weights, out=None, ws=None, stream=None):
+        fn = fused_moe_a16w4 if self.a16 else fused_moe_a8w4
+        return fn(x, topk_ids, topk_weights, self.w1, self.w1_scale, self.w2, self.w2_scale,
+                  out=out, ws=ws, stream=stream)

@@ -1,0 +1,61 @@
+// Internal launch interface between the C-ABI front end (moe_mx.cu) and the
+// kernel translation units. Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Sets the dynamic shared-memory limit of `func` once per device.
+cudaError_t ensure_smem_attr(const void* func, int bytes);
+
+size_t sort_smem_bytes(int E);
+cudaError_t launch_sort(const int32_t* ids, const float* wts, int R, int E, int bm, int64_t p_max,
+                        int32_t* sorted_route, float* sorted_w, int32_t* block_expert,
+                        int32_t* expert_off, int32_t* num_padded, int32_t* route_pos,
+                        int32_t* status, cudaStream_t s);
+
+cudaError_t launch_quant_act(const void* x, int M, int K, int ldx, uint8_t* q, uint8_t* scale,
+                             cudaStream_t s);
+
+cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uint8_t* out,
+                                  cudaStream_t s);
+
+// Gathers the activation rows of the sorted routes (quantised to FP8 with
+// scale atoms for a8w4, copied as BF16 for a16w4), zeroes pad rows, and
+// zeroes the FP32 accumulator [M, H].
+cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, int bm,
+                              int64_t p_max, const int32_t* sorted_route,
+                              const int32_t* num_padded, void* act, uint8_t* act_sf,
+                              float* acc, cudaStream_t s);
+
+cudaError_t launch_finalize(const float* acc, int64_t n, void* out, cudaStream_t s);
+
+struct GemmArgs {
+  bool a16;
+  int M, H, Ip, E, topk, bm;
+  int64_t p_max;
+  const int32_t* sorted_route;
+  const float* sorted_w;
+  const int32_t* block_expert;
+  const int32_t* num_padded;
+  const uint8_t* w1;
+  const uint8_t* w1s;   // prepacked atoms
+  const uint8_t* w2;
+  const uint8_t* w2s;
+  const void* act;      // gathered activations [p_max, H]
+  const uint8_t* act_sf;
+  void* inter;          // [p_max, Ip]
+  uint8_t* inter_sf;
+  float* acc;           // [M, H]
+  int32_t* status;
+};
+
+// tcgen05 block-scaled grouped GEMM, a8w4, stage 1 or 2.
+cudaError_t launch_gemm_mx(int stage, const GemmArgs& a, cudaStream_t s);
+
+cudaError_t launch_stage1_simt(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_stage2_simt(const GemmArgs& a, cudaStream_t s);
+
+}  // namespace moe

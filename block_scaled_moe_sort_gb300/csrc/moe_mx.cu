@@ -1,0 +1,253 @@
+// C-ABI front end of the fused MoE library: argument checks, workspace
+// carving, block_m choice and the launch sequence of one layer call.
+// Declarations and the full contract are in include/moe_mx.h.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <cuda_runtime.h>
+#include "moe_mx.h"
+#include "common.cuh"
+#include "moe_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+cudaError_t ensure_smem_attr(const void* func, int bytes) {
+  // One flag per (device, function); the set of functions is small and fixed.
+  struct Entry { const void* f; int dev; int bytes; };
+  static Entry done[256];
+  static int n_done = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].f == func && done[i].dev == dev && done[i].bytes >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err != cudaSuccess) return err;
+  if (n_done < 256) done[n_done++] = Entry{func, dev, bytes};
+  return cudaSuccess;
+}
+
+namespace {
+
+constexpr int64_t kAlign = 256;
+
+int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) % kAlign) == 0; }
+
+bool valid_bm(int bm) { return bm == 16 || bm == 32 || bm == 64 || bm == 128 || bm == 256; }
+
+// Upper bound of the padded sorted length: every valid route plus at most
+// block_m - 1 pads for each expert that can be non-empty.
+int64_t max_padded(int64_t R, int E, int bm) {
+  const int64_t nonempty = R < E ? R : E;
+  return align_up(R + nonempty * (bm - 1), bm);
+}
+
+// Route block of both GEMMs, from the mean routes per expert.
+int choose_block_m(int M, int topk, int E) {
+  const int64_t per_expert = (static_cast<int64_t>(M) * topk + E - 1) / E;
+  if (per_expert <= 16) return 16;
+  if (per_expert <= 32) return 32;
+  if (per_expert <= 64) return 64;
+  return 128;
+}
+
+moe_status_t check_shape(int M, int H, int Ip, int E, int topk) {
+  if (M < 0 || H <= 0 || Ip <= 0 || E <= 0 || topk <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 128 != 0 || Ip % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (E > kMaxExperts || topk > kMaxTopk) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(M) * topk > (int64_t(1) << 24)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+void build_layout(int M, int H, int Ip, int E, int topk, bool a16, moe_ws_layout_t* L) {
+  std::memset(L, 0, sizeof(*L));
+  const int bm = choose_block_m(M, topk, E);
+  const int64_t R = static_cast<int64_t>(M) * topk;
+  const int64_t pm = max_padded(R, E, bm);
+  const int64_t nblk = pm / bm;
+  const int64_t atoms = (bm + 127) / 128;
+  int64_t o = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t at = o;
+    o = align_up(o + (bytes > 0 ? bytes : 0), kAlign);
+    return at;
+  };
+  L->block_m = bm;
+  L->p_max = pm;
+  L->status_off = take(16);
+  L->expert_off_off = take(4 * (E + 1));
+  L->sorted_route_off = take(4 * pm);
+  L->sorted_w_off = take(4 * pm);
+  L->block_expert_off = take(4 * nblk);
+  L->route_pos_off = take(4 * R);
+  L->act_off = take(pm * H * (a16 ? 2 : 1));
+  L->act_sf_off = take(a16 ? 0 : nblk * (H / 128) * atoms * 512);
+  L->inter_off = take(pm * Ip * (a16 ? 2 : 1));
+  L->inter_sf_off = take(a16 ? 0 : nblk * (Ip / 128) * atoms * 512);
+  L->acc_off = take(static_cast<int64_t>(M) * H * 4);
+  L->total_bytes = o;
+}
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const float* wts, int M,
+                            int H, int topk, const uint8_t* w1, const uint8_t* w1s,
+                            const uint8_t* w2, const uint8_t* w2s, int E, int Ip, void* out,
+                            void* ws, size_t ws_bytes, cudaStream_t s) {
+  moe_status_t st = check_shape(M, H, Ip, E, topk);
+  if (st != MOE_OK) return st;
+  if (!ws || !w1 || !w1s || !w2 || !w2s) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !ids || !wts || !out)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, ids, wts, w1, w1s, w2, w2s, out, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned(p)) return MOE_ERR_ALIGNMENT;
+  moe_ws_layout_t L;
+  build_layout(M, H, Ip, E, topk, a16, &L);
+  if (ws_bytes < static_cast<size_t>(L.total_bytes)) return MOE_ERR_WORKSPACE;
+  if (M == 0) return MOE_OK;
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(base + L.status_off);
+  int32_t* num_padded = status + 1;
+  int32_t* expert_off = reinterpret_cast<int32_t*>(base + L.expert_off_off);
+  int32_t* sorted_route = reinterpret_cast<int32_t*>(base + L.sorted_route_off);
+  float* sorted_w = reinterpret_cast<float*>(base + L.sorted_w_off);
+  int32_t* block_expert = reinterpret_cast<int32_t*>(base + L.block_expert_off);
+  int32_t* route_pos = reinterpret_cast<int32_t*>(base + L.route_pos_off);
+  void* act = base + L.act_off;
+  uint8_t* act_sf = base + L.act_sf_off;
+  void* inter = base + L.inter_off;
+  uint8_t* inter_sf = base + L.inter_sf_off;
+  float* acc = reinterpret_cast<float*>(base + L.acc_off);
+  const int R = M * topk;
+
+  cudaError_t e = launch_sort(ids, wts, R, E, L.block_m, L.p_max, sorted_route, sorted_w,
+                              block_expert, expert_off, num_padded, route_pos, status, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_gather_act(a16, x, M, H, topk, L.block_m, L.p_max, sorted_route, num_padded, act,
+                        act_sf, acc, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  GemmArgs g{};
+  g.a16 = a16;
+  g.M = M; g.H = H; g.Ip = Ip; g.E = E; g.topk = topk; g.bm = L.block_m;
+  g.p_max = L.p_max;
+  g.sorted_route = sorted_route; g.sorted_w = sorted_w; g.block_expert = block_expert;
+  g.num_padded = num_padded;
+  g.w1 = w1; g.w1s = w1s; g.w2 = w2; g.w2s = w2s;
+  g.act = act; g.act_sf = act_sf; g.inter = inter; g.inter_sf = inter_sf; g.acc = acc;
+  g.status = status;
+  e = a16 ? launch_stage1_simt(g, s) : launch_gemm_mx(1, g, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = a16 ? launch_stage2_simt(g, s) : launch_gemm_mx(2, g, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_finalize(acc, static_cast<int64_t>(M) * H, out, s);
+  return from_cuda(e);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_ALIGNMENT: return "pointer not 256-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int64_t moe_sort_max_padded(int M, int topk, int E, int block_m) {
+  if (M < 0 || topk <= 0 || E <= 0 || !valid_bm(block_m)) return -1;
+  return max_padded(static_cast<int64_t>(M) * topk, E, block_m);
+}
+
+moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M, int topk, int E,
+                      int block_m, int32_t* sorted_route, float* sorted_w, int32_t* block_expert,
+                      int32_t* expert_off, int32_t* num_padded, int32_t* route_pos,
+                      moe_stream_t stream) {
+  if (M < 0 || topk <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+  if (!valid_bm(block_m) || E > kMaxExperts || topk > kMaxTopk) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(M) * topk > (int64_t(1) << 24)) return MOE_ERR_UNSUPPORTED;
+  const int64_t pm = max_padded(static_cast<int64_t>(M) * topk, E, block_m);
+  if (!expert_off || !num_padded) return MOE_ERR_INVALID_ARG;
+  if (pm > 0 && (!sorted_route || !sorted_w || !block_expert)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_sort(topk_ids, topk_weights, M * topk, E, block_m, pm, sorted_route,
+                               sorted_w, block_expert, expert_off, num_padded, route_pos, nullptr,
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t* q,
+                              uint8_t* scale, moe_stream_t stream) {
+  if (M < 0 || K <= 0 || ldx < K) return MOE_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldx % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (M > 0 && (!x_bf16 || !q || !scale)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!aligned(x_bf16) || !aligned(q) || !aligned(scale))) return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_quant_act(x_bf16, M, K, ldx, q, scale,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_prepacked_scale_bytes(int E, int N, int K) {
+  if (E <= 0 || N <= 0 || K <= 0 || N % 128 || K % 128) return 0;
+  return static_cast<size_t>(E) * N * (K / 32);
+}
+
+moe_status_t moe_prepack_scales_mx(const uint8_t* scale, int E, int N, int K, uint8_t* out,
+                                   moe_stream_t stream) {
+  if (E <= 0 || N <= 0 || K <= 0 || !scale || !out) return MOE_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(scale) || !aligned(out)) return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_prepack_scales(scale, E, N, K, out,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fused_moe_workspace_bytes(int M, int H, int Ip, int E, int topk, int a16) {
+  if (check_shape(M, H, Ip, E, topk) != MOE_OK) return 0;
+  moe_ws_layout_t L;
+  build_layout(M, H, Ip, E, topk, a16 != 0, &L);
+  return static_cast<size_t>(L.total_bytes);
+}
+
+moe_status_t fused_moe_workspace_layout(int M, int H, int Ip, int E, int topk, int a16,
+                                        moe_ws_layout_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_shape(M, H, Ip, E, topk);
+  if (st != MOE_OK) return st;
+  build_layout(M, H, Ip, E, topk, a16 != 0, out);
+  return MOE_OK;
+}
+
+moe_status_t fused_moe_a8w4(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                            int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                            const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip, void* out,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return fused_moe_impl(false, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
+                        E, Ip, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                             int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                             const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip, void* out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return fused_moe_impl(true, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
+                        E, Ip, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_decode_device_status(int32_t status_word) {
+  return (status_word & kDevTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+}  // extern "C"

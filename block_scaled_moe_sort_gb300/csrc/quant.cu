@@ -1,0 +1,189 @@
+// Memory-bound helpers of the fused MoE layer:
+//  * per-1x32 FP8 activation quantisation (AITER #5609 "Add DeepSeek V4.1
+//    Flash TP4 gfx950 MoE tuning", Configuration: FP8 activations, per-1x32
+//    scaling),
+//  * the gather of each sorted route's token row into route order (quantised
+//    for a8w4, BF16 for a16w4) with its scales in MMA atoms,
+//  * the one-time weight-scale prepack into MMA atoms,
+//  * the FP32 -> BF16 finalisation of the routing-weighted sum.
+// All loops are warp-per-row with 16-byte vector accesses.
+#include <cstdint>
+#include "common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u = __ldg(p + q);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+      v[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_codes32(uint8_t* dst, const uint32_t* c) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+  p[0] = make_uint4(c[0], c[1], c[2], c[3]);
+  p[1] = make_uint4(c[4], c[5], c[6], c[7]);
+}
+
+__global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
+                                                        int M, int K, int ldx,
+                                                        uint8_t* __restrict__ q,
+                                                        uint8_t* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const int nblk = K / 32;
+  const __nv_bfloat16* xr = x + static_cast<int64_t>(row) * ldx;
+  for (int b = lane; b < nblk; b += 32) {
+    float v[32];
+    uint32_t c[8];
+    load_bf16x32(xr + b * 32, v);
+    const uint8_t sb = quant_block32(v, c);
+    store_codes32(q + static_cast<int64_t>(row) * K + b * 32, c);
+    scale[static_cast<int64_t>(row) * nblk + b] = sb;
+  }
+}
+
+template <bool A16>
+__global__ void __launch_bounds__(256) gather_act_kernel(
+    const __nv_bfloat16* __restrict__ x, int M, int H, int topk, int bm, int64_t p_max,
+    const int32_t* __restrict__ sorted_route, const int32_t* __restrict__ num_padded,
+    void* __restrict__ act, uint8_t* __restrict__ act_sf, float* __restrict__ acc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int P = *num_padded;
+  const int R = M * topk;
+  if (p < P) {
+    const int r = __ldg(sorted_route + p);
+    const bool pad = r >= R;
+    const int t = pad ? 0 : r / topk;
+    const __nv_bfloat16* xr = x + static_cast<int64_t>(t) * H;
+    if (A16) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(act) + p * H);
+      const uint4* src = reinterpret_cast<const uint4*>(xr);
+      for (int i = lane; i < H / 8; i += 32) dst[i] = pad ? make_uint4(0, 0, 0, 0) : __ldg(src + i);
+    } else {
+      uint8_t* dst = static_cast<uint8_t*>(act) + p * H;
+      const int blk = static_cast<int>(p / bm), rr = static_cast<int>(p % bm);
+      const int atoms = (bm + 127) / 128;
+      const int nslab = H / 128;
+      for (int b = lane; b < H / 32; b += 32) {
+        uint32_t c[8];
+        uint8_t sb = 0;
+        if (pad) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) c[i] = 0u;
+        } else {
+          float v[32];
+          load_bf16x32(xr + b * 32, v);
+          sb = quant_block32(v, c);
+        }
+        store_codes32(dst + b * 32, c);
+        const int64_t atom = (static_cast<int64_t>(blk) * nslab + b / 4) * atoms + rr / 128;
+        act_sf[atom * 512 + sf_atom_off(rr & 127, b & 3)] = sb;
+      }
+    }
+  }
+  // zero the FP32 routing-weighted accumulator
+  const int64_t n4 = static_cast<int64_t>(M) * H / 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  float4* a4 = reinterpret_cast<float4*>(acc);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+    a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* __restrict__ scale,
+                                                             int E, int N, int K,
+                                                             uint8_t* __restrict__ out) {
+  const int64_t total = static_cast<int64_t>(E) * N * (K / 32);
+  const int nb_n = N / 128, nb_k = K / 128;
+  for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
+       o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int off = static_cast<int>(o & 511);
+    int64_t a = o >> 9;
+    const int kb = static_cast<int>(a % nb_k);
+    a /= nb_k;
+    const int nb = static_cast<int>(a % nb_n);
+    const int e = static_cast<int>(a / nb_n);
+    const int r = (off >> 4) + 32 * ((off & 15) >> 2);
+    const int i = off & 3;
+    out[o] = scale[(static_cast<int64_t>(e) * N + nb * 128 + r) * (K / 32) + kb * 4 + i];
+  }
+}
+
+__global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc, int64_t n8,
+                                                       __nv_bfloat16* __restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+    uint4 u;
+    u.x = *reinterpret_cast<uint32_t*>(&h0);
+    u.y = *reinterpret_cast<uint32_t*>(&h1);
+    u.z = *reinterpret_cast<uint32_t*>(&h2);
+    u.w = *reinterpret_cast<uint32_t*>(&h3);
+    reinterpret_cast<uint4*>(out)[i] = u;
+  }
+}
+
+int grid_for(int64_t work, int per_cta, int cap) {
+  int64_t g = (work + per_cta - 1) / per_cta;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const void* x, int M, int K, int ldx, uint8_t* q, uint8_t* scale,
+                             cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  quant_act_kernel<<<(M + 7) / 8, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), M, K, ldx, q,
+                                               scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, int bm,
+                              int64_t p_max, const int32_t* sorted_route,
+                              const int32_t* num_padded, void* act, uint8_t* act_sf,
+                              float* acc, cudaStream_t s) {
+  const int grid = static_cast<int>((p_max + 7) / 8) > 0 ? static_cast<int>((p_max + 7) / 8) : 1;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (a16)
+    gather_act_kernel<true><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, p_max, sorted_route,
+                                                 num_padded, act, act_sf, acc);
+  else
+    gather_act_kernel<false><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, p_max, sorted_route,
+                                                  num_padded, act, act_sf, acc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uint8_t* out,
+                                  cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(E) * N * (K / 32);
+  if (total == 0) return cudaSuccess;
+  prepack_scales_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, s>>>(scale, E, N, K, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* acc, int64_t n, void* out, cudaStream_t s) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return cudaSuccess;
+  finalize_kernel<<<grid_for(n8, 256, 152 * 8), 256, 0, s>>>(acc, n8,
+                                                              static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

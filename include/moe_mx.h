@@ -1,0 +1,180 @@
+/*
+ * moe_mx.h - C ABI of the GB300 (sm_103a) block-scaled fused MoE layer.
+ *
+ * One call of the layer (a8w4 variant) does, on one CUDA stream:
+ *   sort    token-expert routes grouped by expert, each group padded to
+ *           block_m ("the sorter": AITER #5609 "Add DeepSeek V4.1 Flash TP4
+ *           gfx950 MoE tuning", Performance on the measured runtime; sorting
+ *           is part of the timed call in AITER #5904 "Add tuned a8w4
+ *           fused-MoE configs for DeepSeek V4.1-Flash (TP4 + EP, gfx950)",
+ *           Fused-MoE kernel expert-parallel benchmark)
+ *   quant   BF16 tokens -> FP8 E4M3 + one E8M0 scale per 1x32 along K
+ *           (AITER #5609, Configuration: FP8 activations, per-1x32 scaling)
+ *   stage 1 grouped GEMM against interleaved gate/up MXFP4 expert rows,
+ *           SiLU(gate)*up with no routing-weight multiply, requantised to
+ *           per-1x32 FP8 (AITER #5609, Configuration; "the intermediate
+ *           quantization", AITER #5904, Fused-MoE kernel benchmark)
+ *   stage 2 grouped down-projection GEMM; the routing-weighted sum over a
+ *           token's routes is reduced into a BF16 output (AITER #5609,
+ *           Configuration: BF16 output)
+ * The a16w4 variant keeps BF16 activations and a BF16 intermediate
+ * (AITER #6286 "Retune gfx942 a16w4 DSv4.1 tiles for Triton 3.8", reviewer
+ * reply: moe_gemm_a16w4, w1 with apply_swiglu=True, w2 separate, bf16,
+ * MXFP4).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless stated; the caller owns all memory.
+ *    The library never allocates, frees or synchronises, and never reads
+ *    device data on the host, so every call can be captured in a CUDA graph
+ *    (all launch shapes depend only on the integer arguments).
+ *  - Inputs are const and never written.
+ *  - Argument errors return synchronously before any launch, leaving every
+ *    buffer untouched. Launch failures return MOE_ERR_CUDA (from
+ *    cudaGetLastError). Device-side faults the kernels detect themselves (a
+ *    pipeline wait that timed out) set bits in the workspace status word, see
+ *    moe_ws_layout_t.status_off.
+ *  - Layouts are row-major. E2M1 codes are packed two per byte: element k in
+ *    byte k/2, low nibble = even k. E8M0 scale bytes hold 2^(b-127), one per
+ *    32 consecutive elements along K. In w1 row 2j is gate_j and row 2j+1 is
+ *    up_j. Device pointers must be 256-byte aligned; the stream is a
+ *    cudaStream_t (0 = legacy default stream).
+ */
+#ifndef MOE_MX_H
+#define MOE_MX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size */
+  MOE_ERR_UNSUPPORTED = 2,  /* a shape outside what the kernels implement */
+  MOE_ERR_WORKSPACE = 3,    /* workspace smaller than the *_workspace_bytes size */
+  MOE_ERR_ALIGNMENT = 4,    /* a pointer not 256-byte aligned */
+  MOE_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed */
+  MOE_ERR_TIMEOUT = 6       /* reported by moe_decode_device_status */
+} moe_status_t;
+
+/* Static text for a status code (never NULL). */
+const char* moe_status_string(moe_status_t s);
+
+/* ------------------------------------------------------------------ sort
+ * moe_sort: stable counting sort of the M*topk routes by expert id.
+ * Route r = t*topk + j (token t, slot j) goes to expert topk_ids[r]; routes
+ * whose id is outside [0, E) are dropped (expert-parallel shard). Within an
+ * expert routes keep ascending r. Each non-empty expert's segment is padded
+ * to a multiple of block_m; empty experts take no block.
+ *
+ * Outputs (device, caller-allocated, sizes from moe_sort_max_padded):
+ *   sorted_route [P_max] int32  route r per sorted position; pad = M*topk
+ *   sorted_w     [P_max] float  topk_weights[r]; pad = 0
+ *   block_expert [P_max/block_m] int32  expert of each block_m block; -1
+ *                for blocks at or beyond num_padded
+ *   expert_off   [E+1]   int32  padded segment starts, expert_off[E] = P
+ *   num_padded   [1]     int32  P = sum_e ceil(cnt_e/block_m)*block_m
+ *   route_pos    [M*topk] int32 sorted position of r, -1 if dropped
+ *                (may be NULL)
+ * Positions in [P, P_max) are filled with the pad sentinel. When P_max is 0
+ * (M == 0) the three P_max-sized outputs may be NULL.
+ * Limits: 1 <= E <= 512, 1 <= topk <= 16, block_m in {16,32,64,128,256},
+ * M*topk <= 2^24. M == 0 is allowed (writes the empty result).
+ */
+int64_t moe_sort_max_padded(int M, int topk, int E, int block_m);
+moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M, int topk,
+                      int E, int block_m, int32_t* sorted_route, float* sorted_w,
+                      int32_t* block_expert, int32_t* expert_off, int32_t* num_padded,
+                      int32_t* route_pos, moe_stream_t stream);
+
+/* -------------------------------------------------------- activation quant
+ * moe_quant_act_mx: x BF16 [M, K] (row stride ldx elements) -> q E4M3 codes
+ * [M, K] (row stride K) and scale E8M0 bytes [M, K/32]. Per 1x32 block:
+ * amax == 0 gives scale byte 0 and zero codes; otherwise the scale is
+ * 2^(floor(log2 amax) - 8) clamped to [2^-127, 2^127] and each code is the
+ * round-to-nearest-even E4M3 of x / scale, saturating at +-448.
+ * Limits: K % 32 == 0, ldx >= K, ldx % 8 == 0.
+ */
+moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t* q,
+                              uint8_t* scale, moe_stream_t stream);
+
+/* ---------------------------------------------------- weight scale prepack
+ * The GEMMs read weight scales in 512-byte atoms. moe_prepack_scales_mx
+ * converts row-major scales [E, N, K/32] into [E][N/128][K/128][512]: in the
+ * atom of row block nb and K slab kb, the byte of row r (0..127) and 32-block
+ * i (0..3) sits at (r % 32) * 16 + (r / 32) * 4 + i. Call once at weight-load
+ * time; the output is what fused_moe_* take as w*_scale.
+ * Limits: N % 128 == 0, K % 128 == 0.
+ */
+size_t moe_prepacked_scale_bytes(int E, int N, int K);
+moe_status_t moe_prepack_scales_mx(const uint8_t* scale, int E, int N, int K, uint8_t* out,
+                                   moe_stream_t stream);
+
+/* ---------------------------------------------------------- fused layer
+ * Workspace: fused_moe_workspace_bytes gives the size for the shape; the
+ * caller allocates it (device, 256-byte aligned) and may reuse it for any
+ * later call with the same or a smaller shape. Contents need no
+ * initialisation. Two calls in flight on different streams need different
+ * workspaces.
+ */
+typedef struct {
+  int32_t block_m;       /* route block of both GEMMs (= sort block) */
+  int32_t _pad;
+  int64_t p_max;         /* sorted-list capacity */
+  int64_t status_off;    /* int32[4]: [0] device status bits, [1] num_padded */
+  int64_t expert_off_off;   /* int32 [E+1] */
+  int64_t sorted_route_off; /* int32 [p_max] */
+  int64_t sorted_w_off;     /* float [p_max] */
+  int64_t block_expert_off; /* int32 [p_max/block_m] */
+  int64_t route_pos_off;    /* int32 [M*topk] */
+  int64_t act_off;       /* a8w4: E4M3 [p_max, H] gathered rows; a16w4: BF16 [p_max, H] */
+  int64_t act_sf_off;    /* a8w4: scale atoms [p_max/block_m][H/128][ceil(block_m/128)][512] */
+  int64_t inter_off;     /* a8w4: E4M3 [p_max, Ip]; a16w4: BF16 [p_max, Ip] */
+  int64_t inter_sf_off;  /* a8w4: scale atoms [p_max/block_m][Ip/128][ceil(block_m/128)][512] */
+  int64_t acc_off;       /* float [M, H] routing-weighted sum before BF16 rounding */
+  int64_t total_bytes;
+} moe_ws_layout_t;
+
+size_t fused_moe_workspace_bytes(int M, int H, int Ip, int E, int topk, int a16);
+moe_status_t fused_moe_workspace_layout(int M, int H, int Ip, int E, int topk, int a16,
+                                        moe_ws_layout_t* out /* host */);
+
+/* fused_moe_a8w4: out = MoE(x) with FP8 activations and MXFP4 weights.
+ *   x            BF16 [M, H]
+ *   topk_ids     int32 [M, topk]  (ids outside [0, E) are dropped)
+ *   topk_weights float [M, topk]
+ *   w1           uint8 [E, 2*Ip, H/2]  E2M1, gate/up interleaved rows
+ *   w1_scale     prepacked scales of w1 (moe_prepack_scales_mx with N=2*Ip, K=H)
+ *   w2           uint8 [E, H, Ip/2]    E2M1
+ *   w2_scale     prepacked scales of w2 (N=H, K=Ip)
+ *   out          BF16 [M, H]
+ * Ip is the stored (padded) intermediate size; padding rows/columns of the
+ * weights must hold zero codes. Tokens without a local route get 0.
+ * Limits: H % 128 == 0, Ip % 128 == 0, 1 <= E <= 512, 1 <= topk <= 16,
+ * 0 <= M, M*topk <= 2^24.
+ */
+moe_status_t fused_moe_a8w4(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                            int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                            const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip, void* out,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* fused_moe_a16w4: as fused_moe_a8w4 with BF16 activations (no activation
+ * quantisation) and a BF16 intermediate. Same arguments and limits. */
+moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids,
+                             const float* topk_weights, int M, int H, int topk,
+                             const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
+                             const uint8_t* w2_scale, int E, int Ip, void* out, void* ws,
+                             size_t ws_bytes, moe_stream_t stream);
+
+/* Decode the status word copied from the workspace (host value) into a
+ * moe_status_t: MOE_OK, or MOE_ERR_TIMEOUT if a device wait gave up. */
+moe_status_t moe_decode_device_status(int32_t status_word);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_MX_H */

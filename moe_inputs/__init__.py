@@ -40,6 +40,7 @@ from __future__ import annotations
 import dataclasses
 from typing import Optional
 
+import numpy as np
 import torch
 
 H_DSV41 = 5120
@@ -169,17 +170,25 @@ def make_routing(shape: MoeShape, M: int, g: torch.Generator, mode: str = "unifo
     return ids, w
 
 
-def _codes(n_rows: int, n_bytes: int, g: torch.Generator) -> torch.Tensor:
-    return torch.randint(0, 256, (n_rows, n_bytes), generator=g, dtype=torch.uint8)
+def _codes(n_rows: int, n_bytes: int, rng: np.random.Generator) -> torch.Tensor:
+    # uniform bytes (both nibbles uniform over the 16 E2M1 codes), taken from
+    # the raw 64-bit PCG64 stream, little-endian
+    n = n_rows * n_bytes
+    raw = rng.bit_generator.random_raw((n + 7) // 8)
+    buf = raw.view(np.uint8)[:n]
+    return torch.from_numpy(buf).view(n_rows, n_bytes)
 
 
-def _scales(n_rows: int, n_blocks: int, g: torch.Generator) -> torch.Tensor:
-    return (127 + torch.randint(-8, -3, (n_rows, n_blocks), generator=g,
-                                dtype=torch.int16)).to(torch.uint8)
+def _scales(n_rows: int, n_blocks: int, rng: np.random.Generator) -> torch.Tensor:
+    # E8M0 exponents uniform in [-8, -4]
+    v = rng.integers(127 - 8, 127 - 3, size=(n_rows, n_blocks), dtype=np.uint8)
+    return torch.from_numpy(v)
 
 
-def make_weights(shape: MoeShape, g: torch.Generator, experts: Optional[int] = None):
-    """MXFP4 expert weights in the canonical byte layout (see module doc)."""
+def make_weights(shape: MoeShape, seed: int, experts: Optional[int] = None):
+    """MXFP4 expert weights in the canonical byte layout (see module doc).
+    Drawn with numpy's PCG64 (platform-independent) for speed."""
+    g = np.random.Generator(np.random.PCG64(seed))
     E = shape.E if experts is None else experts
     H, I, Ip = shape.H, shape.I, shape.Ip
     w1 = _codes(E * 2 * Ip, H // 2, g).view(E, 2 * Ip, H // 2)
@@ -218,7 +227,7 @@ def make_case(shape_name: str, M: int, variant: int = 0, routing: str = "uniform
     if routing == "hot":
         variant = max(variant, 1)
     if weights is None:
-        weights = make_weights(shp, _gen(weight_seed(cfg, variant)))
+        weights = make_weights(shp, weight_seed(cfg, variant))
     seed = call_seed(cfg, M, variant)
     g = _gen(seed)
     x = make_x(M, shp.H, g)

@@ -1,0 +1,147 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the
+C-ABI binding and compare it with the CPU oracle on the same seeded inputs.
+
+Bars (from the layer's specification): sorted route lists and padding
+bit-exact; activation quantisation bit-exact; >= 99.9% of the stage-one
+intermediate codes identical; BF16 output within atol = rtol = 2e-2 of the
+oracle, with the max abs error reported.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import block_scaled_moe_sort_gb300 as m
+import moe_inputs as mi
+from oracle import moe as om
+from oracle import mx_formats as mx
+
+ATOL = 2e-2
+RTOL = 2e-2
+CODE_MATCH = 0.999
+
+
+@functools.lru_cache(maxsize=4)
+def weights_for(shape_name: str, variant: int = 0):
+    shp = mi.SHAPES[shape_name]
+    cfg = mi.CONFIG_INDEX[shape_name]
+    return mi.make_weights(shp, mi.weight_seed(cfg, variant))
+
+
+@functools.lru_cache(maxsize=4)
+def layer_for(shape_name: str, variant: int = 0):
+    w = weights_for(shape_name, variant)
+    return m.MoeLayer(w["w1"], w["w1_scale"], w["w2"], w["w2_scale"],
+                      a16=mi.SHAPES[shape_name].a16)
+
+
+def ws_slice(ws: torch.Tensor, off: int, dtype, count: int) -> torch.Tensor:
+    nbytes = count * torch.empty(0, dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype)
+
+
+def untile_sf(atoms: np.ndarray, p: np.ndarray, nblocks: int, K: int, bm: int) -> np.ndarray:
+    """Scale bytes [len(p), nblocks] from the 512-byte MMA atom layout."""
+    na = (bm + 127) // 128
+    p = p.astype(np.int64)[:, None]
+    i = np.arange(nblocks, dtype=np.int64)[None, :]
+    rr = p % bm
+    atom = ((p // bm) * (K // 128) + i // 4) * na + rr // 128
+    off = atom * 512 + (rr % 32) * 16 + ((rr % 128) // 32) * 4 + i % 4
+    return atoms[off]
+
+
+def run_case(layer: m.MoeLayer, case: mi.MoeCase, poison: bool = True):
+    M, k = case.M, case.topk_ids.shape[1]
+    dev = "cuda"
+    x = case.x.to(dev)
+    ids = case.topk_ids.to(dev)
+    w = case.topk_weights.to(dev)
+    nbytes = layer.workspace_bytes(M, k)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty(M, layer.H, dtype=torch.bfloat16, device=dev)
+    if poison:
+        ws.fill_(0xFF)
+        out.view(torch.int16).fill_(-1)
+    layer(x, ids, w, out=out, ws=ws)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+def compare(case: mi.MoeCase, layer: m.MoeLayer, a16: bool, tokens=None, check_inter=True):
+    """Run GPU + oracle; assert every bar; return a stats dict."""
+    out, ws = run_case(layer, case)
+    M, k = case.M, case.topk_ids.shape[1]
+    E, H, Ip = layer.E, layer.H, layer.Ip
+    lay = m.fused_moe_workspace_layout(M, H, Ip, E, k, a16)
+    bm, pm = lay["block_m"], lay["p_max"]
+    ref = om.fused_moe(case.x, case.topk_ids, case.topk_weights, case.w1, case.w1_scale,
+                       case.w2, case.w2_scale, E, a16=a16, block_m=bm, tokens=tokens)
+    wsc = ws.cpu()
+    status = ws_slice(wsc, lay["status_off"], torch.int32, 4).numpy()
+    assert status[0] == 0, f"device status {status[0]}"
+    # ---- sort: bit-exact, including the sentinel tail
+    srt = ref.sort
+    P = srt.num_padded
+    assert status[1] == P
+    got_route = ws_slice(wsc, lay["sorted_route_off"], torch.int32, pm).numpy()
+    got_w = ws_slice(wsc, lay["sorted_w_off"], torch.float32, pm).numpy()
+    got_be = ws_slice(wsc, lay["block_expert_off"], torch.int32, pm // bm).numpy()
+    got_off = ws_slice(wsc, lay["expert_off_off"], torch.int32, E + 1).numpy()
+    got_pos = ws_slice(wsc, lay["route_pos_off"], torch.int32, M * k).numpy()
+    assert np.array_equal(got_route[:P], srt.sorted_route)
+    assert (got_route[P:] == M * k).all()
+    assert np.array_equal(got_w[:P].view(np.uint32), srt.sorted_w.view(np.uint32))
+    assert np.array_equal(got_be[:P // bm], srt.block_expert)
+    assert (got_be[P // bm:] == -1).all()
+    assert np.array_equal(got_off, srt.expert_off)
+    assert np.array_equal(got_pos, srt.route_pos)
+    stats = dict(M=M, block_m=bm, P=int(P))
+    # ---- stage-one intermediate, valid rows: >= 99.9 % identical codes
+    rows = ref.inter_rows
+    if check_inter and rows.size:
+        if a16:
+            inter = ws_slice(wsc, lay["inter_off"], torch.bfloat16, pm * Ip).view(pm, Ip)
+            got = inter[torch.from_numpy(rows)].to(torch.float64).numpy()
+            same = (got == ref.aq)
+            stats["inter_match"] = float(same.mean())
+        else:
+            inter = ws_slice(wsc, lay["inter_off"], torch.uint8, pm * Ip).view(pm, Ip).numpy()
+            got = inter[rows]
+            same = (got == ref.aq)
+            sf_atoms = wsc[lay["inter_sf_off"]:].numpy()
+            got_sf = untile_sf(sf_atoms, rows, Ip // 32, Ip, bm)
+            stats["inter_match"] = float(same.mean())
+            stats["inter_sf_match"] = float((got_sf == ref.as_).mean())
+            assert stats["inter_sf_match"] >= CODE_MATCH, stats
+        assert stats["inter_match"] >= CODE_MATCH, stats
+        # pad rows of the intermediate hold zeros
+        pad_rows = np.nonzero(got_route[:P] == M * k)[0]
+        if pad_rows.size:
+            pr = torch.from_numpy(pad_rows)
+            if a16:
+                assert (inter[pr].to(torch.float32) == 0).all()
+            else:
+                assert (inter[pad_rows] == 0).all()
+    # ---- output
+    got_out = out.cpu()
+    sel = ref.tokens
+    o = got_out[torch.from_numpy(sel)].to(torch.float64).numpy()
+    want = ref.out_bf16
+    err = np.abs(o - want)
+    stats["max_abs_err"] = float(err.max()) if err.size else 0.0
+    stats["out_exact"] = float((o == want).mean()) if err.size else 1.0
+    bad = err > ATOL + RTOL * np.abs(want)
+    assert not bad.any(), dict(stats, n_bad=int(bad.sum()), worst=float(err.max()))
+    assert np.isfinite(got_out.to(torch.float32).numpy()).all()
+    return stats
+
+
+def sample_tokens(M: int, n: int, seed: int) -> np.ndarray:
+    if M <= n:
+        return np.arange(M)
+    g = np.random.default_rng(seed)
+    pick = g.choice(M, size=n - 2, replace=False)
+    return np.unique(np.concatenate([[0, M - 1], pick]))

@@ -1,0 +1,98 @@
+"""The C-ABI library loads without a GPU, exports every function the header
+declares, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+
+import pytest
+
+import block_scaled_moe_sort_gb300 as m
+from block_scaled_moe_sort_gb300 import build as b
+
+
+@pytest.fixture(scope="module")
+def L():
+    b.build()
+    return m.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = m.declared_functions()
+    for want in ["moe_sort", "moe_quant_act_mx", "fused_moe_a8w4", "fused_moe_a16w4",
+                 "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "moe_status_string"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    raw = ctypes.CDLL(b.LIB)
+    missing = [n for n in m.declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.moe_status_string(code)
+    assert L.moe_status_string(3) == b"workspace too small"
+
+
+FAKE = 0x10000  # an aligned host-side address; never dereferenced on error paths
+
+
+def _call(L, fn, M=4, H=256, topk=2, E=8, Ip=128, ws=FAKE, ws_bytes=1 << 40, x=FAKE, ids=FAKE,
+          w=FAKE, w1=FAKE, w1s=FAKE, w2=FAKE, w2s=FAKE, out=FAKE):
+    return getattr(L, fn)(x, ids, w, M, H, topk, w1, w1s, w2, w2s, E, Ip, out, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("fn", ["fused_moe_a8w4", "fused_moe_a16w4"])
+def test_fused_rejects_bad_arguments_on_host(L, fn):
+    assert _call(L, fn, ws=None) == 1                 # null workspace
+    assert _call(L, fn, x=None) == 1                  # null input with M > 0
+    assert _call(L, fn, M=-1) == 1
+    assert _call(L, fn, H=200) == 2                   # H % 128
+    assert _call(L, fn, Ip=96) == 2                   # Ip % 128
+    assert _call(L, fn, E=513) == 2
+    assert _call(L, fn, topk=17) == 2
+    assert _call(L, fn, out=FAKE + 16) == 4           # misaligned
+    assert _call(L, fn, ws_bytes=16) == 3             # workspace too small
+    assert _call(L, fn, M=0, x=None, ids=None, w=None, out=None) == 0  # empty call, no launch
+
+
+def test_workspace_size_and_layout(L):
+    for a16 in (0, 1):
+        n = L.fused_moe_workspace_bytes(96, 5120, 640, 384, 6, a16)
+        lay = m.fused_moe_workspace_layout(96, 5120, 640, 384, 6, bool(a16))
+        assert n == lay["total_bytes"] > 0
+        offs = [lay[k] for k in ("status_off", "expert_off_off", "sorted_route_off",
+                                 "sorted_w_off", "block_expert_off", "route_pos_off", "act_off",
+                                 "inter_off", "acc_off")]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+        assert lay["block_m"] in (16, 32, 64, 128, 256)
+        assert lay["p_max"] % lay["block_m"] == 0
+        assert lay["acc_off"] + 96 * 5120 * 4 <= n
+    assert L.fused_moe_workspace_bytes(4, 200, 128, 8, 2, 0) == 0
+
+
+def test_sort_capacity_bound(L):
+    # every route plus block_m - 1 pads per possibly non-empty expert
+    assert L.moe_sort_max_padded(5, 3, 128, 16) == 15 + 15 * 15
+    assert L.moe_sort_max_padded(1000, 6, 384, 64) == -(-(6000 + 384 * 63) // 64) * 64
+    assert L.moe_sort_max_padded(0, 6, 384, 64) == 0
+    assert L.moe_sort_max_padded(4, 2, 8, 24) == -1   # unsupported block
+
+
+def test_sort_and_quant_reject_bad_arguments(L):
+    args = [FAKE, FAKE, 4, 2, 8, 16, FAKE, FAKE, FAKE, FAKE, FAKE, None, None]
+    bad = list(args); bad[5] = 48
+    assert L.moe_sort(*bad) == 2
+    bad = list(args); bad[4] = 600
+    assert L.moe_sort(*bad) == 2
+    bad = list(args); bad[6] = None
+    assert L.moe_sort(*bad) == 1
+    assert L.moe_quant_act_mx(FAKE, 4, 100, 100, FAKE, FAKE, None) == 2   # K % 32
+    assert L.moe_quant_act_mx(FAKE, 4, 128, 64, FAKE, FAKE, None) == 1    # ldx < K
+    assert L.moe_quant_act_mx(FAKE + 8, 4, 128, 128, FAKE, FAKE, None) == 4
+    assert L.moe_prepack_scales_mx(FAKE, 2, 100, 256, FAKE, None) == 2
+    assert L.moe_prepacked_scale_bytes(2, 256, 512) == 2 * 256 * 16
+
+
+def test_device_status_decoding(L):
+    assert L.moe_decode_device_status(0) == 0
+    assert L.moe_decode_device_status(1) == 6

@@ -1,0 +1,98 @@
+"""GPU parity of the whole fused MoE call against the oracle.
+
+Small geometries are compared in full (every token, every intermediate row);
+the pages' geometries (draft, backbone incl. the M31/32/33/255/256/257
+boundary checks and concentrated routing, expert-parallel shard, a16w4
+384-top6 and 385-top7 with the fused shared expert, Zipf prefill stress) are
+compared on every route of a seeded sample of tokens, at the sizes and in the
+launch configuration the benchmark uses. Workspace and output are poisoned
+(0xFF) before each call, so anything left unwritten shows up.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_moe_sort_gb300 as m
+import moe_inputs as mi
+from moe_check import compare, layer_for, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def _small_layer(shp, seed):
+    w = mi.make_weights(shp, seed)
+    return w, m.MoeLayer(w["w1"], w["w1_scale"], w["w2"], w["w2_scale"], a16=shp.a16)
+
+
+@pytest.mark.parametrize("a16", [False, True])
+@pytest.mark.parametrize("M", [1, 5, 37, 130, 600])
+def test_small_geometry_full(cuda_lib, a16, M):
+    shp = mi.small_shape(H=512, I=192, Ip=256, E=8, topk=3, E_route=10, a16=a16)
+    w, layer = _small_layer(shp, 5)
+    case = mi.make_case("small", M, shape=shp, weights=w)
+    st = compare(case, layer, a16)
+    print(st)
+
+
+def test_empty_experts_and_all_dropped_tokens(cuda_lib):
+    shp = mi.small_shape(H=256, I=128, Ip=128, E=16, topk=2, E_route=64)
+    w, layer = _small_layer(shp, 9)
+    case = mi.make_case("small", 20, shape=shp, weights=w)
+    assert ((case.topk_ids >= 16).all(dim=1)).any()   # some tokens have no local route
+    compare(case, layer, False)
+
+
+def test_zero_tokens(cuda_lib):
+    shp = mi.small_shape(H=256, I=128, Ip=128, E=4, topk=2)
+    w, layer = _small_layer(shp, 3)
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(0, 2, dtype=torch.int32, device="cuda")
+    wt = torch.empty(0, 2, dtype=torch.float32, device="cuda")
+    out = layer(x, ids, wt)
+    assert out.shape == (0, 256)
+
+
+def _config_case(name, M, routing="uniform", variant=0, n_tok=8):
+    layer = layer_for(name, variant)
+    case = mi.make_case(name, M, variant=variant, routing=routing,
+                        weights=__import__("moe_check").weights_for(name, variant))
+    return layer, case, sample_tokens(M, n_tok, M + variant)
+
+
+@pytest.mark.parametrize("M", [5])
+def test_draft(cuda_lib, M):
+    layer, case, tok = _config_case("draft", M)
+    print(compare(case, layer, False, tokens=None))
+
+
+@pytest.mark.parametrize("M", [6, 96, 768, 31, 32, 33, 255, 256, 257])
+def test_backbone(cuda_lib, M):
+    layer, case, tok = _config_case("backbone", M)
+    print(compare(case, layer, False, tokens=None if M <= 6 else tok))
+
+
+def test_backbone_concentrated_routing(cuda_lib):
+    layer, case, tok = _config_case("backbone", 384, routing="hot", variant=1)
+    print(compare(case, layer, False, tokens=tok))
+
+
+@pytest.mark.parametrize("M", [1, 16, 1024, 16384])
+def test_expert_parallel_shard(cuda_lib, M):
+    layer, case, tok = _config_case("ep", M)
+    print(compare(case, layer, False, tokens=None if M <= 16 else tok))
+
+
+@pytest.mark.parametrize("name", ["a16w4_384", "a16w4_385"])
+@pytest.mark.parametrize("M", [12, 1024])
+def test_a16w4(cuda_lib, name, M):
+    layer, case, tok = _config_case(name, M)
+    print(compare(case, layer, True, tokens=None if M <= 12 else tok))
+
+
+def test_zipf_prefill_stress(cuda_lib):
+    layer = layer_for("backbone")
+    w = __import__("moe_check").weights_for("backbone")
+    case = mi.make_case("backbone", 16384, routing="zipf", weights=w)
+    counts = np.bincount(case.topk_ids.reshape(-1).numpy(), minlength=384)
+    assert counts.max() > 20 * np.median(counts)
+    print(compare(case, layer, False, tokens=sample_tokens(16384, 8, 4)))
