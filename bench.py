@@ -1,0 +1,358 @@
+"""Benchmark of the GB300 block-scaled fused MoE layer.
+
+Default workload (one "step" = one whole fused_moe_a8w4 call: sort,
+activation quantisation, stage-1 GEMM + SiLU/requant, stage-2 GEMM +
+weighted reduction, BF16 output): the DeepSeek-V4.1-Flash TP4 backbone MoE
+at the largest decode bucket of its sweep, M=768 tokens, H=5120,
+I=576 padded to 640, 384 experts, top-6, uniform routing, seeded synthetic
+inputs (AITER #5609 "Add DeepSeek V4.1 Flash TP4 gfx950 MoE tuning",
+Configuration). The other buckets of that sweep are reported under "sweep".
+
+Timing: the call is captured once in a CUDA graph; every timed step flushes
+L2 (a 256 MiB write, outside the timed events) and replays the graph between
+two CUDA events on the launching stream. W untimed warm-up steps come first;
+exactly K steps are timed inside a barrier + synchronize bracket, max over
+ranks. A second pass of K eager calls records events around each kernel
+(moe_profile_*) for the roofline of the dominant kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--M 768]
+  python bench.py --impl reference     # the CPU oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "fused_moe us/call (backbone a8w4 decode, M=768)"
+SWEEP = mi.TOKENS["backbone"]
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def work_model(shape, ids, M):
+    """Algorithmic bytes and flops of one call (valid routes, touched experts)."""
+    E, H, Ip, k = shape.E, shape.H, shape.Ip, ids.shape[1]
+    flat = ids.reshape(-1)
+    valid = flat[(flat >= 0) & (flat < E)]
+    R = int(valid.numel())
+    Et = int(torch.unique(valid).numel())
+    w1_e = 2 * Ip * (H // 2 + H // 32)
+    w2_e = H * (Ip // 2 + Ip // 32)
+    s1 = Et * w1_e + R * H * (1 + 1 / 32) + R * Ip * (1 + 1 / 32)
+    s2 = Et * w2_e + R * Ip * (1 + 1 / 32) + M * H * 4
+    call = Et * (w1_e + w2_e) + M * H * 2 * 2 + 2 * R * Ip * (1 + 1 / 32)
+    flops = 2.0 * R * (2 * Ip * H + H * Ip)
+    return dict(R=R, experts_touched=Et, stage1_bytes=s1, stage2_bytes=s2, call_bytes=call,
+                flops=flops)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [ln.split(",") for ln in open(self.path).read().splitlines() if ln.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip() == "Active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(case, shape, budget_s: float = 12.0):
+    """Time the FP64 oracle on a bounded slice (whole experts) of the call and
+    scale to the full call by the touched-expert count."""
+    from oracle import moe as om
+    flat = case.topk_ids.reshape(-1)
+    touched = torch.unique(flat[(flat >= 0) & (flat < shape.E)]).tolist()
+    done, t_used = 0, 0.0
+    chunk = 4
+    while done < len(touched) and t_used < budget_s:
+        sel = touched[done:done + chunk]
+        t0 = time.perf_counter()
+        om.fused_moe(case.x, case.topk_ids, case.topk_weights, case.w1, case.w1_scale,
+                     case.w2, case.w2_scale, shape.E, a16=shape.a16, experts=sel)
+        t_used += time.perf_counter() - t0
+        done += len(sel)
+    est_us = t_used / done * len(touched) * 1e6
+    return {"value": round(est_us, 1), "unit": "us/call", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": (f"FP64 numpy oracle on {done} of the {len(touched)} touched experts "
+                       f"(all their routes) of the M={case.M} call, {t_used:.1f} s, scaled by "
+                       f"{len(touched)}/{done}; BLAS threads = host cores")}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    shape = mi.SHAPES["backbone"]
+    case = mi.make_case("backbone", args.M)
+    for _ in range(args.warmup):
+        cpu_baseline(case, shape, budget_s=1.0)
+    budget = max(1.0, min(args.ref_budget, 150.0 / (args.steps + args.warmup)))
+    vals = [cpu_baseline(case, shape, budget_s=budget) for _ in range(args.steps)]
+    v = statistics.mean(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = round(v, 1)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/call",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(v / 1000, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": config_dict(args.M, world), "cpu_baseline": cb,
+            "e2e": {"value": round(v, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(M, world):
+    return {"workload": f"DeepSeek-V4.1-Flash TP4 backbone MoE a8w4 decode bucket M={M}: "
+                        "H=5120, I=576 padded to 640, 384 experts, top-6, uniform routing",
+            "tokens": M, "H": 5120, "I": 576, "Ip": 640, "experts": 384, "topk": 6,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed (256 MiB write) before every timed step"}
+
+
+def time_graph(layer, x, ids, w, out, ws, steps, warmup, flush, stream):
+    for _ in range(warmup):
+        layer(x, ids, w, out=out, ws=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        layer(x, ids, w, out=out, ws=ws)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--M", type=int, default=768)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_scaled_moe_sort_gb300 as m
+
+    shape = mi.SHAPES["backbone"]
+    weights = mi.make_weights(shape, mi.weight_seed(1))
+    layer = m.MoeLayer(weights["w1"], weights["w1_scale"], weights["w2"], weights["w2_scale"],
+                       device=dev)
+    case = mi.make_case("backbone", args.M, weights=weights)
+    x, ids, w = case.x.to(dev), case.topk_ids.to(dev), case.topk_weights.to(dev)
+    M, k = args.M, shape.topk
+    out = torch.empty(M, shape.H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(layer.workspace_bytes(M, k), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    hbm, _, peak_kind = peaks()
+    wm = work_model(shape, case.topk_ids, M)
+
+    with torch.cuda.stream(stream):
+        g = time_graph(layer, x, ids, w, out, ws, args.steps, args.warmup, flush, stream)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(local)
+        sampler.start()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            g.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clocks = sampler.stop()
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        total_ms = sum(step_ms)
+        if world > 1:
+            t = torch.tensor([total_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            total_ms = float(t.item())
+        us_per_call = total_ms * 1000 / (args.steps * world)
+
+        # ---- per-kernel timing pass (eager calls, events around each kernel)
+        m.moe_profile_enable(True)
+        m.moe_profile_collect()
+        for i in range(args.steps):
+            flush.zero_()
+            layer(x, ids, w, out=out, ws=ws)
+        torch.cuda.synchronize()
+        kms, ncalls = m.moe_profile_collect()
+        m.moe_profile_enable(False)
+        kmean = {kk: v / max(ncalls, 1) for kk, v in kms.items()}
+
+        # ---- end to end through the public API with host buffers
+        xh = case.x.pin_memory()
+        idh = case.topk_ids.pin_memory()
+        wh = case.topk_weights.pin_memory()
+        oh = torch.empty(M, shape.H, dtype=torch.bfloat16).pin_memory()
+        e_s = torch.cuda.Event(enable_timing=True)
+        e_e = torch.cuda.Event(enable_timing=True)
+        e2e_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e_s.record(stream)
+            x.copy_(xh, non_blocking=True)
+            ids.copy_(idh, non_blocking=True)
+            w.copy_(wh, non_blocking=True)
+            layer(x, ids, w, out=out, ws=ws)
+            oh.copy_(out, non_blocking=True)
+            e_e.record(stream)
+            e_e.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(e_s.elapsed_time(e_e))
+        e2e_us = statistics.mean(e2e_ms) * 1000
+
+        # ---- decode sweep of the same geometry
+        sweep = {}
+        if not args.no_sweep:
+            for Ms in SWEEP:
+                c = mi.make_case("backbone", Ms, weights=weights)
+                xs, ids_s, w_s = c.x.to(dev), c.topk_ids.to(dev), c.topk_weights.to(dev)
+                o_s = torch.empty(Ms, shape.H, dtype=torch.bfloat16, device=dev)
+                ws_s = torch.empty(layer.workspace_bytes(Ms, k), dtype=torch.uint8, device=dev)
+                gs = time_graph(layer, xs, ids_s, w_s, o_s, ws_s, 5, 3, flush, stream)
+                ts = []
+                for _ in range(10):
+                    flush.zero_()
+                    e_s.record(stream)
+                    gs.replay()
+                    e_e.record(stream)
+                    e_e.synchronize()
+                    ts.append(e_s.elapsed_time(e_e))
+                us = statistics.median(ts) * 1000
+                wms = work_model(shape, c.topk_ids, Ms)
+                sweep[str(Ms)] = {"us": round(us, 2),
+                                  "tflops": round(wms["flops"] / us / 1e6, 2),
+                                  "hbm_frac": round(wms["call_bytes"] / us / 1e3 / hbm, 3)}
+                del gs
+
+    # ---- roofline of the dominant kernel
+    dom = max(("stage1_gemm", "stage2_gemm"), key=lambda kk: kmean[kk])
+    dom_bytes = wm["stage1_bytes"] if dom == "stage1_gemm" else wm["stage2_bytes"]
+    dom_ms = kmean[dom]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+            "algorithmic_bytes": int(dom_bytes), "kernel_us": round(dom_ms * 1000, 2)}
+
+    line = {
+        "metric": METRIC, "value": round(us_per_call, 2), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 x mxfp4 (fp32 accumulate)",
+        "data": "synthetic (seeded, random-init weights)", "config": config_dict(M, world),
+        "tflops": round(wm["flops"] / us_per_call / 1e6, 2),
+        "call_hbm_frac": round(wm["call_bytes"] / us_per_call / 1e3 / hbm, 4),
+        "kernels_us": {kk: round(v * 1000, 2) for kk, v in kmean.items()},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_us, 2), "unit": "us/call",
+                "h2d_bytes_per_step": int(x.numel() * 2 + ids.numel() * 4 + w.numel() * 4),
+                "d2h_bytes_per_step": int(out.numel() * 2)},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+        "work": wm,
+    }
+    if sweep:
+        line["sweep"] = sweep
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, shape)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

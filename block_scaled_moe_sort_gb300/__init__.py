@@ -21,6 +21,7 @@ __all__ = [
     "lib", "MoeError", "moe_sort", "moe_sort_max_padded", "moe_quant_act_mx",
     "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
+    "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS",
 ]
 
 HEADER = os.path.join(_build.ROOT, "include", "moe_mx.h")
@@ -58,7 +59,12 @@ _SIGS = {
                                  _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
                                  _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
     "moe_decode_device_status": (_c_int, [ctypes.c_int32]),
+    "moe_profile_enable": (_c_int, [_c_int]),
+    "moe_profile_collect": (_c_int, [ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_int32)]),
 }
+
+PROFILE_SLOTS = ("sort", "gather_quant", "stage1_gemm", "stage2_gemm", "finalize")
 
 _LIB = None
 
@@ -224,6 +230,19 @@ def fused_moe_a16w4(x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
     """BF16-activation x MXFP4-weight fused MoE; returns BF16 [M, H]."""
     return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
                   w2_scale_packed, out, ws, stream)
+
+
+def moe_profile_enable(enable: bool = True) -> None:
+    _check("moe_profile_enable", lib().moe_profile_enable(int(enable)))
+
+
+def moe_profile_collect() -> tuple:
+    """Summed milliseconds per kernel slot of the calls since the last
+    collect, and the number of calls (see moe_mx.h)."""
+    ms = (ctypes.c_double * len(PROFILE_SLOTS))()
+    n = ctypes.c_int32(0)
+    _check("moe_profile_collect", lib().moe_profile_collect(ms, ctypes.byref(n)))
+    return dict(zip(PROFILE_SLOTS, list(ms))), int(n.value)
 
 
 class MoeLayer:

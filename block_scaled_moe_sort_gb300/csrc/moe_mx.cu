@@ -95,6 +95,34 @@ void build_layout(int M, int H, int Ip, int E, int topk, bool a16, moe_ws_layout
 
 moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// ---------------------------------------------------------------- timing
+constexpr int kProfSlots = MOE_PROFILE_SLOTS;
+constexpr int kProfMaxCalls = 1024;
+struct Profiler {
+  bool enabled = false;
+  int pending = 0;
+  int dropped = 0;
+  cudaEvent_t ev[kProfMaxCalls][2 * kProfSlots] = {};
+  bool created[kProfMaxCalls] = {};
+};
+Profiler g_prof;
+
+// Records the begin (before=true) or end event of `slot` for the current call.
+void prof_mark(int slot, bool before, cudaStream_t s) {
+  if (!g_prof.enabled || g_prof.pending >= kProfMaxCalls) return;
+  const int c = g_prof.pending;
+  if (!g_prof.created[c]) {
+    for (int i = 0; i < 2 * kProfSlots; ++i) cudaEventCreate(&g_prof.ev[c][i]);
+    g_prof.created[c] = true;
+  }
+  cudaEventRecord(g_prof.ev[c][2 * slot + (before ? 0 : 1)], s);
+}
+void prof_end_call() {
+  if (!g_prof.enabled) return;
+  if (g_prof.pending < kProfMaxCalls) ++g_prof.pending;
+  else ++g_prof.dropped;
+}
+
 moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const float* wts, int M,
                             int H, int topk, const uint8_t* w1, const uint8_t* w1s,
                             const uint8_t* w2, const uint8_t* w2s, int E, int Ip, void* out,
@@ -126,12 +154,16 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   float* acc = reinterpret_cast<float*>(base + L.acc_off);
   const int R = M * topk;
 
+  prof_mark(0, true, s);
   cudaError_t e = launch_sort(ids, wts, R, E, L.block_m, L.p_max, sorted_route, sorted_w,
                               block_expert, expert_off, num_padded, route_pos, status, s);
   if (e != cudaSuccess) return from_cuda(e);
+  prof_mark(0, false, s);
+  prof_mark(1, true, s);
   e = launch_gather_act(a16, x, M, H, topk, L.block_m, L.p_max, sorted_route, num_padded, act,
                         act_sf, acc, s);
   if (e != cudaSuccess) return from_cuda(e);
+  prof_mark(1, false, s);
   GemmArgs g{};
   g.a16 = a16;
   g.M = M; g.H = H; g.Ip = Ip; g.E = E; g.topk = topk; g.bm = L.block_m;
@@ -141,12 +173,20 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   g.w1 = w1; g.w1s = w1s; g.w2 = w2; g.w2s = w2s;
   g.act = act; g.act_sf = act_sf; g.inter = inter; g.inter_sf = inter_sf; g.acc = acc;
   g.status = status;
+  prof_mark(2, true, s);
   e = a16 ? launch_stage1_simt(g, s) : launch_gemm_mx(1, g, s);
   if (e != cudaSuccess) return from_cuda(e);
+  prof_mark(2, false, s);
+  prof_mark(3, true, s);
   e = a16 ? launch_stage2_simt(g, s) : launch_gemm_mx(2, g, s);
   if (e != cudaSuccess) return from_cuda(e);
+  prof_mark(3, false, s);
+  prof_mark(4, true, s);
   e = launch_finalize(acc, static_cast<int64_t>(M) * H, out, s);
-  return from_cuda(e);
+  if (e != cudaSuccess) return from_cuda(e);
+  prof_mark(4, false, s);
+  prof_end_call();
+  return MOE_OK;
 }
 
 }  // namespace
@@ -244,6 +284,28 @@ moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids, const float
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   return fused_moe_impl(true, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
                         E, Ip, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_profile_enable(int enable) {
+  g_prof.enabled = enable != 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_profile_collect(double* kernel_ms, int32_t* n_calls) {
+  if (!kernel_ms || !n_calls) return MOE_ERR_INVALID_ARG;
+  for (int c = 0; c < g_prof.pending; ++c) {
+    if (cudaEventSynchronize(g_prof.ev[c][2 * kProfSlots - 1]) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int k = 0; k < kProfSlots; ++k) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, g_prof.ev[c][2 * k], g_prof.ev[c][2 * k + 1]) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      kernel_ms[k] += ms;
+    }
+  }
+  *n_calls = g_prof.pending;
+  g_prof.pending = 0;
+  g_prof.dropped = 0;
+  return MOE_OK;
 }
 
 moe_status_t moe_decode_device_status(int32_t status_word) {

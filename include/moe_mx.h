@@ -170,6 +170,22 @@ moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids,
                              const uint8_t* w2_scale, int E, int Ip, void* out, void* ws,
                              size_t ws_bytes, moe_stream_t stream);
 
+/* --------------------------------------------------------- kernel timing
+ * For benchmarks and profiling. While enabled, every fused_moe_* call records
+ * a CUDA event right before and right after each of its kernel launches, on
+ * the call's stream (slot 0 sort, 1 activation gather/quant, 2 stage-1 GEMM,
+ * 3 stage-2 GEMM, 4 BF16 finalise). moe_profile_collect waits for those
+ * events, adds each slot's elapsed milliseconds into kernel_ms[slot] (an
+ * array of MOE_PROFILE_SLOTS doubles, host), writes the number of calls
+ * measured to *n_calls and forgets them. Off by default; the events are
+ * created on first use and kept. Up to 1024 calls may be pending; later
+ * calls are not recorded. Not thread-safe; do not enable it while capturing
+ * a CUDA graph.
+ */
+#define MOE_PROFILE_SLOTS 5
+moe_status_t moe_profile_enable(int enable);
+moe_status_t moe_profile_collect(double* kernel_ms, int32_t* n_calls);
+
 /* Decode the status word copied from the workspace (host value) into a
  * moe_status_t: MOE_OK, or MOE_ERR_TIMEOUT if a device wait gave up. */
 moe_status_t moe_decode_device_status(int32_t status_word);
