@@ -1,0 +1,451 @@
+// Grouped GEMMs of the a16w4 fused MoE layer (BF16 activations x MXFP4
+// weights; AITER #6286 "Retune gfx942 a16w4 DSv4.1 tiles for Triton 3.8",
+// reviewer reply: moe_gemm_a16w4 with w1 apply_swiglu=True, w2 separate,
+// bf16, MXFP4) on tcgen05.mma kind::f16 with TMEM accumulators:
+//
+//   stage 1: D[n, p] = sum_k W1[e][n, k] * X[p, k]; epilogue SiLU(gate)*up,
+//            rounded to a BF16 intermediate
+//   stage 2: D[n, p] = sum_k W2[e][n, k] * A[p, k]; epilogue
+//            acc[token(p), n] += w_p * D[n, p]
+//
+// kind::f16 needs both operands in the same 16-bit type, so the MXFP4
+// weights are dequantised in shared memory: every E2M1 value times its E8M0
+// scale is a BF16 number (exact: a 2-bit-mantissa value times a power of two),
+// so the MMA sees exactly the weights the format encodes.
+//
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
+// issuer, warps 2..5 epilogue (TMEM lane quadrant = warp % 4), warps 6..9
+// converters (one weight row per thread: packed FP4 + scale -> 128-byte
+// swizzled K-major BF16, the layout the MMA descriptor reads).
+// Pipeline stage = 64 K-elements (one 128-byte swizzle atom of BF16).
+#include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include "common.cuh"
+#include "moe_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kTileN = 128;   // weight rows per tile (MMA M)
+constexpr int kTileK = 64;    // K per stage
+constexpr int kMmaK = 16;     // K per tcgen05.mma kind::f16
+
+struct Bf16Args {
+  int stage;
+  int M, topk, H, Ip, E;
+  int N, K;
+  int n_tiles;
+  int num_blocks;
+  const int32_t* sorted_route;
+  const float* sorted_w;
+  const int32_t* block_expert;
+  const int32_t* num_padded;
+  const uint8_t* sfa;          // weight scale atoms [E][N/128][K/128][512]
+  __nv_bfloat16* inter;        // stage 1 out: BF16 [p_max, Ip]
+  float* acc;                  // stage 2 out
+  int32_t* status;
+};
+
+template <int BN>
+struct Cfg16 {
+  static constexpr int kRawBytes = kTileN * kTileK / 2;        // 4 KB packed FP4
+  static constexpr int kSfBytes = 512;
+  static constexpr int kBBytes = BN * kTileK * 2;              // BF16 routes
+  static constexpr int kABytes = kTileN * kTileK * 2;          // 16 KB BF16 weights
+  // layout inside a stage: A (1024-aligned), B (1024-aligned), raw, sf
+  static constexpr int kStageBytes = (kABytes + kBBytes + kRawBytes + kSfBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = BN <= 64 ? 6 : (BN <= 128 ? 5 : 3);
+  static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
+  static constexpr int kColsNeeded = kAccBufs * BN;
+  static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64
+                                   : kColsNeeded <= 128 ? 128 : kColsNeeded <= 256 ? 256 : 512;
+  static constexpr int kEpiFloats = 32 * (64 + 4);
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiFloats * 4 + 256;
+  static constexpr uint32_t kTxBytes = kRawBytes + kSfBytes + kBBytes;
+  static_assert(kSmem <= 227 * 1024, "smem budget");
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
+  __nv_bfloat162 z = __hmul2(x, y);
+  return *reinterpret_cast<uint32_t*>(&z);
+}
+
+// Four E2M1 codes (code i in bits 4i..4i+3 of p16) -> four BF16 values times
+// the power-of-two scale held twice in scale2. The magnitude of each code is
+// looked up byte-wise (high and low byte of its BF16 pattern, 3-bit index),
+// the sign is bit 3 of the code; the scaling multiply is exact.
+__device__ __forceinline__ void fp4x4_to_bf16(uint32_t p16, uint32_t scale2, uint32_t& w01,
+                                              uint32_t& w23) {
+  const uint32_t sel = p16 & 0x7777u;
+  // |E2M1| = 0, .5, 1, 1.5, 2, 3, 4, 6 -> BF16 0000 3F00 3F80 3FC0 4000 4040 4080 40C0
+  const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel);
+  const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);
+  uint32_t a = prmt(lo, hi, 0x5140u);
+  uint32_t b = prmt(lo, hi, 0x7362u);
+  a |= ((p16 << 12) & 0x8000u) | ((p16 << 24) & 0x80000000u);
+  b |= ((p16 << 4) & 0x8000u) | ((p16 << 16) & 0x80000000u);
+  w01 = bf16x2_mul(a, scale2);
+  w23 = bf16x2_mul(b, scale2);
+}
+
+__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t s) {
+  const uint32_t h = s == 0 ? 0x0040u : (s << 7);   // 2^(s-127) as BF16 (s=0: subnormal)
+  return h | (h << 16);
+}
+
+__device__ __forceinline__ void tile_coords(int t, const Bf16Args& a, int& m_blk, int& n_tile) {
+  if (a.stage == 1) {
+    m_blk = t / a.n_tiles;
+    n_tile = t % a.n_tiles;
+  } else {
+    n_tile = t / a.num_blocks;
+    m_blk = t % a.num_blocks;
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_bf16w4_kernel(const __grid_constant__ CUtensorMap tmW,
+                           const __grid_constant__ CUtensorMap tmX, const Bf16Args a) {
+  using C = Cfg16<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  float* epi = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  __shared__ uint64_t full_bar[C::kStages], conv_bar[C::kStages], empty_bar[C::kStages];
+  __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
+  __shared__ uint64_t drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = *a.num_padded;
+  const int total_tiles = a.num_blocks * a.n_tiles;
+  const int kblocks = a.K / kTileK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&conv_bar[s], 4);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  auto stage_ptr = [&](int s) { return smem + s * C::kStageBytes; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        int m_blk, n_tile;
+        tile_coords(t, a, m_blk, n_tile);
+        if (m_blk * BN >= P) continue;
+        const int e = __ldg(a.block_expert + m_blk);
+        if (e < 0 || e >= a.E) continue;
+        const int row_w = e * a.N + n_tile * kTileN;
+        const uint8_t* sfa =
+            a.sfa + ((static_cast<int64_t>(e) * a.n_tiles + n_tile) * (a.K / 128)) * 512;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
+          uint8_t* sb = stage_ptr(stage);
+          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+          tma_load_2d(sb + C::kABytes + C::kBBytes, &tmW, &full_bar[stage], kb * (kTileK / 2),
+                      row_w, pol_w);
+          tma_load_2d(sb + C::kABytes, &tmX, &full_bar[stage], kb * kTileK, m_blk * BN, pol_x);
+          bulk_load(sb + C::kABytes + C::kBBytes + C::kRawBytes, sfa + (kb / 2) * 512, 512,
+                    &full_bar[stage], pol_w);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      constexpr uint32_t idesc = idesc_dense(1, 1, kTileN, BN);
+      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
+        int m_blk, n_tile;
+        tile_coords(t, a, m_blk, n_tile);
+        if (m_blk * BN >= P) continue;
+        const int e = __ldg(a.block_expert + m_blk);
+        if (e < 0 || e >= a.E) continue;
+        const int ab = local % C::kAccBufs;
+        const uint32_t acc_phase = (local / C::kAccBufs) & 1;
+        ++local;
+        if (!mbar_wait(&acc_empty[ab], acc_phase ^ 1, a.status)) { abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + ab * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, a.status) ||
+              !mbar_wait(&conv_bar[stage], phase, a.status)) { abort_flag = 1; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_ptr(stage));
+          const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
+            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(b_addr + kk * 32, 16, 1024, kSwizzle128B);
+            mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
+        tc_commit(&acc_full[ab]);
+      }
+      tc_commit(&drain_bar);
+      mbar_wait(&drain_bar, 0, a.status);
+    }
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------- converters
+    const int r = threadIdx.x - 192;                     // weight row 0..127
+    const int sf_off = sf_atom_off(r, 0);                // its 4 scale bytes
+    const int sw = r & 7;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      int m_blk, n_tile;
+      tile_coords(t, a, m_blk, n_tile);
+      if (m_blk * BN >= P) continue;
+      const int e = __ldg(a.block_expert + m_blk);
+      if (e < 0 || e >= a.E) continue;
+      bool stop = false;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (abort_flag || !mbar_wait(&full_bar[stage], phase, a.status)) {
+          abort_flag = 1; stop = true; break;
+        }
+        uint8_t* sb = stage_ptr(stage);
+        const uint4* raw = reinterpret_cast<const uint4*>(sb + C::kABytes + C::kBBytes + r * 32);
+        const uint32_t sfw = *reinterpret_cast<const uint32_t*>(sb + C::kABytes + C::kBBytes +
+                                                               C::kRawBytes + sf_off);
+        const int i0 = (kb & 1) * 2;                     // 32-blocks of this stage in the atom
+        const uint32_t s0 = e8m0_bf16x2((sfw >> (8 * i0)) & 0xFF);
+        const uint32_t s1 = e8m0_bf16x2((sfw >> (8 * (i0 + 1))) & 0xFF);
+        uint8_t* dst_row = sb + r * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {                    // 32 elements per half
+          const uint4 q = raw[h];
+          const uint32_t sc = h == 0 ? s0 : s1;
+          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {                  // 8 elements -> one 16-byte chunk
+            uint32_t o0, o1, o2, o3;
+            fp4x4_to_bf16(words[j] & 0xFFFFu, sc, o0, o1);
+            fp4x4_to_bf16(words[j] >> 16, sc, o2, o3);
+            const int c = h * 4 + j;                     // chunk index 0..7 in the row
+            *reinterpret_cast<uint4*>(dst_row + ((c ^ sw) << 4)) = make_uint4(o0, o1, o2, o3);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_bar[stage]);
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+      }
+      if (stop) break;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int et = threadIdx.x - 64;
+    const int R = a.M * a.topk;
+    int local = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      int m_blk, n_tile;
+      tile_coords(t, a, m_blk, n_tile);
+      if (m_blk * BN >= P) continue;
+      const int e = __ldg(a.block_expert + m_blk);
+      if (e < 0 || e >= a.E) continue;
+      const int ab = local % C::kAccBufs;
+      const uint32_t acc_phase = (local / C::kAccBufs) & 1;
+      ++local;
+      if (abort_flag || !mbar_wait(&acc_full[ab], acc_phase, a.status)) { abort_flag = 1; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
+      const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
+      constexpr int kChunk = BN < 32 ? BN : 32;
+      for (int c0 = 0; c0 < BN; c0 += kChunk) {
+        float v[32];
+        {
+          uint32_t r32[32];
+          if constexpr (kChunk == 32) {
+            tmem_ld_32x32b_x32(d_tmem + c0, r32);
+          } else {
+            uint32_t r16[16];
+            tmem_ld_32x32b_x16(d_tmem + c0, r16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r32[i] = r16[i];
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r32[i]);
+        }
+        if (a.stage == 1) {
+          const int j_local = row >> 1;
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int i = 0; i < kChunk; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
+            if ((lane & 1) == 0) epi[i * 68 + j_local] = silu_mul(v[i], other);
+          }
+          named_bar_sync(1, 128);
+          const int item = et >> 1, half = et & 1;
+          const int col = item >> 1, blk = item & 1;
+          if (col < kChunk) {
+            const int64_t p = p_base + c0 + col;
+            const bool pad = __ldg(a.sorted_route + p) >= R;
+            const float4* src =
+                reinterpret_cast<const float4*>(epi + col * 68 + blk * 32 + half * 16);
+            uint32_t o[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 f = src[q];
+              __nv_bfloat162 h0 = __floats2bfloat162_rn(f.x, f.y);
+              __nv_bfloat162 h1 = __floats2bfloat162_rn(f.z, f.w);
+              o[2 * q] = pad ? 0u : *reinterpret_cast<uint32_t*>(&h0);
+              o[2 * q + 1] = pad ? 0u : *reinterpret_cast<uint32_t*>(&h1);
+            }
+            const int jcol = n_tile * 64 + blk * 32 + half * 16;
+            uint4* dst = reinterpret_cast<uint4*>(a.inter + p * a.Ip + jcol);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        } else {
+          int tok = -1;
+          float wgt = 0.f;
+          if (lane < kChunk) {
+            const int64_t p = p_base + c0 + lane;
+            const int rr = __ldg(a.sorted_route + p);
+            if (rr < R) { tok = rr / a.topk; wgt = __ldg(a.sorted_w + p); }
+          }
+          const int n = n_tile * kTileN + row;
+#pragma unroll
+          for (int i = 0; i < kChunk; ++i) {
+            const int ti = __shfl_sync(0xffffffffu, tok, i);
+            const float wi = __shfl_sync(0xffffffffu, wgt, i);
+            if (ti >= 0) atomicAdd(a.acc + static_cast<int64_t>(ti) * a.H + n, wi * v[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+               uint64_t rows, uint64_t stride_bytes, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle sw) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess || q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& tw, const CUtensorMap& tx, const Bf16Args& a,
+                      cudaStream_t s) {
+  using C = Cfg16<BN>;
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN>),
+                                     C::kSmem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int tiles = a.num_blocks * a.n_tiles;
+  const int grid = tiles < sms ? tiles : sms;
+  if (grid <= 0) return cudaSuccess;
+  moe_gemm_bf16w4_kernel<BN><<<grid, kThreads, C::kSmem, s>>>(tw, tx, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16w4(int stage, const GemmArgs& g, cudaStream_t s) {
+  Bf16Args a{};
+  a.stage = stage;
+  a.M = g.M; a.topk = g.topk; a.H = g.H; a.Ip = g.Ip; a.E = g.E;
+  a.N = stage == 1 ? 2 * g.Ip : g.H;
+  a.K = stage == 1 ? g.H : g.Ip;
+  a.n_tiles = a.N / kTileN;
+  a.num_blocks = static_cast<int>(g.p_max / g.bm);
+  a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
+  a.num_padded = g.num_padded;
+  a.sfa = stage == 1 ? g.w1s : g.w2s;
+  a.inter = static_cast<__nv_bfloat16*>(g.inter);
+  a.acc = g.acc;
+  a.status = g.status;
+  if (a.num_blocks == 0) return cudaSuccess;
+  CUtensorMap tw, tx;
+  const uint8_t* w = stage == 1 ? g.w1 : g.w2;
+  const void* xb = stage == 1 ? g.act : g.inter;
+  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, a.K / 2,
+                 static_cast<uint64_t>(a.E) * a.N, a.K / 2, kTileK / 2, kTileN,
+                 CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a.K, static_cast<uint64_t>(g.p_max),
+                 static_cast<uint64_t>(a.K) * 2, kTileK, g.bm, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  switch (g.bm) {
+    case 16: return launch_bn<16>(tw, tx, a, s);
+    case 32: return launch_bn<32>(tw, tx, a, s);
+    case 64: return launch_bn<64>(tw, tx, a, s);
+    case 128: return launch_bn<128>(tw, tx, a, s);
+    case 256: return launch_bn<256>(tw, tx, a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

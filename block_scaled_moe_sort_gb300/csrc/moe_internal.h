@@ -54,6 +54,8 @@ struct GemmArgs {
 
 // tcgen05 block-scaled grouped GEMM, a8w4, stage 1 or 2.
 cudaError_t launch_gemm_mx(int stage, const GemmArgs& a, cudaStream_t s);
+// tcgen05 BF16 x (MXFP4 dequantised in shared memory) grouped GEMM, a16w4.
+cudaError_t launch_gemm_bf16w4(int stage, const GemmArgs& a, cudaStream_t s);
 
 cudaError_t launch_stage1_simt(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_stage2_simt(const GemmArgs& a, cudaStream_t s);

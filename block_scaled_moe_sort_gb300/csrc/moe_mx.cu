@@ -174,11 +174,11 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   g.act = act; g.act_sf = act_sf; g.inter = inter; g.inter_sf = inter_sf; g.acc = acc;
   g.status = status;
   prof_mark(2, true, s);
-  e = a16 ? launch_stage1_simt(g, s) : launch_gemm_mx(1, g, s);
+  e = a16 ? launch_gemm_bf16w4(1, g, s) : launch_gemm_mx(1, g, s);
   if (e != cudaSuccess) return from_cuda(e);
   prof_mark(2, false, s);
   prof_mark(3, true, s);
-  e = a16 ? launch_stage2_simt(g, s) : launch_gemm_mx(2, g, s);
+  e = a16 ? launch_gemm_bf16w4(2, g, s) : launch_gemm_mx(2, g, s);
   if (e != cudaSuccess) return from_cuda(e);
   prof_mark(3, false, s);
   prof_mark(4, true, s);
