@@ -21,7 +21,7 @@ __all__ = [
     "lib", "MoeError", "moe_sort", "moe_sort_max_padded", "moe_quant_act_mx",
     "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
-    "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS",
+    "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS", "fused_moe_a8w4_noalloc",
 ]
 
 HEADER = os.path.join(_build.ROOT, "include", "moe_mx.h")
@@ -59,6 +59,9 @@ _SIGS = {
                                  _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
                                  _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
     "moe_decode_device_status": (_c_int, [ctypes.c_int32]),
+    "fused_moe_a8w4_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                        _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
+                                        _c_int, _c_void_p, _c_void_p]),
     "moe_profile_enable": (_c_int, [_c_int]),
     "moe_profile_collect": (_c_int, [ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_int32)]),
@@ -230,6 +233,29 @@ def fused_moe_a16w4(x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
     """BF16-activation x MXFP4-weight fused MoE; returns BF16 [M, H]."""
     return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
                   w2_scale_packed, out, ws, stream)
+
+
+NOALLOC_WORKSPACE_BYTES = 16 << 20
+
+
+def fused_moe_a8w4_noalloc(x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
+                           w2_scale_packed, out=None, stream=None) -> torch.Tensor:
+    """fused_moe_a8w4 without a caller workspace: the library's own static
+    scratch of NOALLOC_WORKSPACE_BYTES is used instead (see moe_mx.h for who
+    needs this, the size limit and why overlapping calls must be avoided)."""
+    M, H = x.shape
+    topk = topk_ids.shape[1]
+    E = w1.shape[0]
+    Ip = w2.shape[2] * 2
+    assert x.dtype == torch.bfloat16 and topk_ids.dtype == torch.int32
+    assert topk_weights.dtype == torch.float32 and w1.dtype == torch.uint8
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
+    code = lib().fused_moe_a8w4_noalloc(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, H, topk, _ptr(w1), _ptr(w1_scale_packed),
+        _ptr(w2), _ptr(w2_scale_packed), E, Ip, _ptr(out), _stream(stream))
+    _check("fused_moe_a8w4_noalloc", code)
+    return out
 
 
 def moe_profile_enable(enable: bool = True) -> None:

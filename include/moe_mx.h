@@ -170,6 +170,36 @@ moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids,
                              const uint8_t* w2_scale, int E, int Ip, void* out, void* ws,
                              size_t ws_bytes, moe_stream_t stream);
 
+/* ------------------------------------------------ no-allocation variant
+ * fused_moe_a8w4_noalloc: fused_moe_a8w4 without a caller workspace. The
+ * pages have no counterpart of this entry point; it exists for callers that
+ * cannot hand the library scratch memory, such as a plugin inside an engine
+ * that owns every device allocation and gives its plugins no way to ask for
+ * more, or a latency-critical path that may not call a device allocator.
+ * The caller still provides every input, the weights and the output.
+ *
+ * The scratch is one static device array of MOE_NOALLOC_WORKSPACE_BYTES
+ * inside this library; each GPU that loads the library keeps it until the
+ * process exits. Shapes whose fused_moe_workspace_bytes() exceeds that size
+ * are rejected with MOE_ERR_WORKSPACE before anything is launched (with the
+ * current workspace layout that is up to 23 tokens at H=5120, Ip=640, 384
+ * experts, top-6, and up to 69 tokens at 128 experts, top-3).
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture on the device. All calls share the one array and it keeps
+ * the previous call's contents (no part of it needs to start at zero), so
+ * calls that can overlap on the GPU (different streams, or different host
+ * threads) race on it: serialise them. Arguments, limits, layouts and errors
+ * are otherwise those of fused_moe_a8w4.
+ */
+#define MOE_NOALLOC_WORKSPACE_BYTES (16u << 20)
+moe_status_t fused_moe_a8w4_noalloc(const void* x, const int32_t* topk_ids,
+                                    const float* topk_weights, int M, int H, int topk,
+                                    const uint8_t* w1, const uint8_t* w1_scale,
+                                    const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                                    void* out, moe_stream_t stream);
+
 /* --------------------------------------------------------- kernel timing
  * For benchmarks and profiling. While enabled, every fused_moe_* call records
  * a CUDA event right before and right after each of its kernel launches, on
