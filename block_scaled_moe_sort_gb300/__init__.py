@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "lib", "MoeError", "moe_sort", "moe_sort_max_padded", "moe_quant_act_mx",
-    "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
+    "moe_prepack_scales_mx", "moe_prepack_weights_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
     "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS", "fused_moe_a8w4_noalloc",
 ]
@@ -37,6 +37,7 @@ class MoeWsLayout(ctypes.Structure):
                 ("status_off", _c_int64), ("expert_off_off", _c_int64),
                 ("sorted_route_off", _c_int64), ("sorted_w_off", _c_int64),
                 ("block_expert_off", _c_int64), ("route_pos_off", _c_int64),
+                ("sort_scratch_off", _c_int64),
                 ("act_off", _c_int64), ("act_sf_off", _c_int64), ("inter_off", _c_int64),
                 ("inter_sf_off", _c_int64), ("acc_off", _c_int64), ("total_bytes", _c_int64)]
 
@@ -44,11 +45,16 @@ class MoeWsLayout(ctypes.Structure):
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_c_int]),
     "moe_sort_max_padded": (_c_int64, [_c_int, _c_int, _c_int, _c_int]),
+    "moe_sort_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
     "moe_sort": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_void_p,
-                          _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+                          _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                          _c_size_t, _c_void_p]),
     "moe_quant_act_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_void_p,
                                   _c_void_p]),
     "moe_prepacked_scale_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
+    "moe_prepacked_weight_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
+    "moe_prepack_weights_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p,
+                                        _c_void_p]),
     "moe_prepack_scales_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_void_p]),
     "fused_moe_workspace_bytes": (_c_size_t, [_c_int] * 6),
     "fused_moe_workspace_layout": (_c_int, [_c_int] * 6 + [ctypes.POINTER(MoeWsLayout)]),
@@ -149,11 +155,13 @@ def moe_sort(topk_ids: torch.Tensor, topk_weights: torch.Tensor, E: int, block_m
         num_padded=torch.empty(1, dtype=torch.int32, device=dev),
         route_pos=torch.empty(M * topk, dtype=torch.int32, device=dev),
     )
+    nws = int(lib().moe_sort_workspace_bytes(M, topk, E, block_m))
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev) if nws else None
     code = lib().moe_sort(_ptr(topk_ids), _ptr(topk_weights), M, topk, E, block_m,
                           out["sorted_route"].data_ptr(), out["sorted_w"].data_ptr(),
                           out["block_expert"].data_ptr() if pm else None,
                           out["expert_off"].data_ptr(), out["num_padded"].data_ptr(),
-                          _ptr(out["route_pos"]), _stream(stream))
+                          _ptr(out["route_pos"]), _ptr(ws), nws, _stream(stream))
     _check("moe_sort", code)
     return out
 
@@ -169,6 +177,20 @@ def moe_quant_act_mx(x: torch.Tensor, stream=None):
     _check("moe_quant_act_mx", lib().moe_quant_act_mx(_ptr(x), M, K, K, _ptr(q), _ptr(s),
                                                       _stream(stream)))
     return q, s
+
+
+def moe_prepack_weights_mx(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """Row-major packed E2M1 codes [E, N, K/2] -> 8 KB weight tiles."""
+    assert w.dtype == torch.uint8 and w.dim() == 3
+    E, N, KH = w.shape
+    K = KH * 2
+    nbytes = int(lib().moe_prepacked_weight_bytes(E, N, K))
+    if nbytes == 0:
+        raise ValueError("unsupported weight shape (N and K must be multiples of 128)")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    _check("moe_prepack_weights_mx", lib().moe_prepack_weights_mx(_ptr(w), E, N, K, _ptr(out),
+                                                                  _stream(stream)))
+    return out
 
 
 def moe_prepack_scales_mx(scale: torch.Tensor, stream=None) -> torch.Tensor:
@@ -199,15 +221,13 @@ def fused_moe_workspace_layout(M: int, H: int, Ip: int, E: int, topk: int, a16: 
 
 
 def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
-           out=None, ws=None, stream=None):
+           E, Ip, out=None, ws=None, stream=None):
     M, H = x.shape
     topk = topk_ids.shape[1]
-    E = w1.shape[0]
-    Ip = w2.shape[2] * 2
     a16 = fn_name == "fused_moe_a16w4"
     assert x.dtype == torch.bfloat16 and topk_ids.dtype == torch.int32
     assert topk_weights.dtype == torch.float32 and w1.dtype == torch.uint8
-    assert w1.shape == (E, 2 * Ip, H // 2) and w2.shape == (E, H, Ip // 2)
+    assert w1.numel() == E * 2 * Ip * H // 2 and w2.numel() == E * H * Ip // 2
     if out is None:
         out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
     if ws is None:
@@ -221,32 +241,32 @@ def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
     return out
 
 
-def fused_moe_a8w4(x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
-                   out=None, ws=None, stream=None) -> torch.Tensor:
-    """FP8-activation x MXFP4-weight fused MoE; returns BF16 [M, H]."""
-    return _fused("fused_moe_a8w4", x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
-                  w2_scale_packed, out, ws, stream)
+def fused_moe_a8w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
+                   w2_scale_packed, E, Ip, out=None, ws=None, stream=None) -> torch.Tensor:
+    """FP8-activation x MXFP4-weight fused MoE on prepacked weights; returns
+    BF16 [M, H]."""
+    return _fused("fused_moe_a8w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream)
 
 
-def fused_moe_a16w4(x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
-                    out=None, ws=None, stream=None) -> torch.Tensor:
-    """BF16-activation x MXFP4-weight fused MoE; returns BF16 [M, H]."""
-    return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
-                  w2_scale_packed, out, ws, stream)
+def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
+                    w2_scale_packed, E, Ip, out=None, ws=None, stream=None) -> torch.Tensor:
+    """BF16-activation x MXFP4-weight fused MoE on prepacked weights; returns
+    BF16 [M, H]."""
+    return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream)
 
 
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
 def fused_moe_a8w4_noalloc(x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
-                           w2_scale_packed, out=None, stream=None) -> torch.Tensor:
+                           w2_scale_packed, E, Ip, out=None, stream=None) -> torch.Tensor:
     """fused_moe_a8w4 without a caller workspace: the library's own static
     scratch of NOALLOC_WORKSPACE_BYTES is used instead (see moe_mx.h for who
     needs this, the size limit and why overlapping calls must be avoided)."""
     M, H = x.shape
     topk = topk_ids.shape[1]
-    E = w1.shape[0]
-    Ip = w2.shape[2] * 2
     assert x.dtype == torch.bfloat16 and topk_ids.dtype == torch.int32
     assert topk_weights.dtype == torch.float32 and w1.dtype == torch.uint8
     if out is None:
@@ -276,13 +296,13 @@ class MoeLayer:
 
     def __init__(self, w1, w1_scale, w2, w2_scale, a16: bool = False, device="cuda"):
         self.a16 = a16
-        self.w1 = w1.to(device).contiguous()
-        self.w2 = w2.to(device).contiguous()
+        self.E = w1.shape[0]
+        self.H = w2.shape[1]
+        self.Ip = w2.shape[2] * 2
+        self.w1 = moe_prepack_weights_mx(w1.to(device).contiguous())
+        self.w2 = moe_prepack_weights_mx(w2.to(device).contiguous())
         self.w1_scale = moe_prepack_scales_mx(w1_scale.to(device).contiguous())
         self.w2_scale = moe_prepack_scales_mx(w2_scale.to(device).contiguous())
-        self.E = self.w1.shape[0]
-        self.H = self.w2.shape[1]
-        self.Ip = self.w2.shape[2] * 2
 
     def workspace_bytes(self, M: int, topk: int) -> int:
         return fused_moe_workspace_bytes(M, self.H, self.Ip, self.E, topk, self.a16)
@@ -290,4 +310,4 @@ class MoeLayer:
     def __call__(self, x, topk_ids, topk_weights, out=None, ws=None, stream=None):
         fn = fused_moe_a16w4 if self.a16 else fused_moe_a8w4
         return fn(x, topk_ids, topk_weights, self.w1, self.w1_scale, self.w2, self.w2_scale,
-                  out=out, ws=ws, stream=stream)
+                  self.E, self.Ip, out=out, ws=ws, stream=stream)

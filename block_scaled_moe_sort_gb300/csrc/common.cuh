@@ -7,7 +7,7 @@
 
 namespace moe {
 
-constexpr int kMaxExperts = 512;
+constexpr int kMaxExperts = 512;   // expert ids fit 9 bits (route sort)
 constexpr int kMaxTopk = 16;
 
 // Byte offset of (row r, 32-block i) inside a 128-row x 4-block scale atom:

@@ -17,8 +17,10 @@
 // issuer, warps 2..5 epilogue (TMEM lane quadrant = warp % 4), warps 6..9
 // converters (one weight row per thread: packed FP4 + scale -> 128-byte
 // swizzled K-major BF16, the layout the MMA descriptor reads).
-// Pipeline stage = 64 K-elements (one 128-byte swizzle atom of BF16).
+// Pipeline stage = 128 K-elements: one prepacked 8 KB weight tile, fetched by
+// a single bulk copy, and two 128-byte swizzle atoms of BF16 per operand.
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include "common.cuh"
@@ -30,8 +32,9 @@ namespace {
 
 constexpr int kThreads = 320;
 constexpr int kTileN = 128;   // weight rows per tile (MMA M)
-constexpr int kTileK = 64;    // K per stage
+constexpr int kTileK = 128;   // K per stage = one prepacked 8 KB weight tile
 constexpr int kMmaK = 16;     // K per tcgen05.mma kind::f16
+constexpr int kAtomK = 64;    // BF16 elements per 128-byte swizzle atom row
 
 struct Bf16Args {
   int stage;
@@ -43,6 +46,7 @@ struct Bf16Args {
   const float* sorted_w;
   const int32_t* block_expert;
   const int32_t* num_padded;
+  const uint8_t* w;            // prepacked E2M1 tiles [E][N/128][K/128][128][64 B]
   const uint8_t* sfa;          // weight scale atoms [E][N/128][K/128][512]
   __nv_bfloat16* inter;        // stage 1 out: BF16 [p_max, Ip]
   float* acc;                  // stage 2 out
@@ -51,13 +55,15 @@ struct Bf16Args {
 
 template <int BN>
 struct Cfg16 {
-  static constexpr int kRawBytes = kTileN * kTileK / 2;        // 4 KB packed FP4
+  static constexpr int kRawBytes = kTileN * kTileK / 2;        // 8 KB packed FP4
   static constexpr int kSfBytes = 512;
-  static constexpr int kBBytes = BN * kTileK * 2;              // BF16 routes
-  static constexpr int kABytes = kTileN * kTileK * 2;          // 16 KB BF16 weights
-  // layout inside a stage: A (1024-aligned), B (1024-aligned), raw, sf
+  static constexpr int kBAtomBytes = BN * 128;                 // BN rows x 64 BF16
+  static constexpr int kBBytes = 2 * kBAtomBytes;
+  static constexpr int kAAtomBytes = kTileN * 128;             // 128 rows x 64 BF16
+  static constexpr int kABytes = 2 * kAAtomBytes;              // 32 KB BF16 weights
+  // stage layout: A atoms (1024-aligned), B atoms (1024-aligned), raw, scales
   static constexpr int kStageBytes = (kABytes + kBBytes + kRawBytes + kSfBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN <= 64 ? 6 : (BN <= 128 ? 5 : 3);
+  static constexpr int kStages = BN <= 32 ? 4 : (BN <= 64 ? 3 : 2);
   static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
   static constexpr int kColsNeeded = kAccBufs * BN;
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64
@@ -147,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmW);
     prefetch_tmap(&tmX);
   }
   if (warp == 1) {
@@ -174,18 +179,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (m_blk * BN >= P) continue;
         const int e = __ldg(a.block_expert + m_blk);
         if (e < 0 || e >= a.E) continue;
-        const int row_w = e * a.N + n_tile * kTileN;
-        const uint8_t* sfa =
-            a.sfa + ((static_cast<int64_t>(e) * a.n_tiles + n_tile) * (a.K / 128)) * 512;
+        const int64_t tile0 = (static_cast<int64_t>(e) * a.n_tiles + n_tile) * kblocks;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
           uint8_t* sb = stage_ptr(stage);
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-          tma_load_2d(sb + C::kABytes + C::kBBytes, &tmW, &full_bar[stage], kb * (kTileK / 2),
-                      row_w, pol_w);
-          tma_load_2d(sb + C::kABytes, &tmX, &full_bar[stage], kb * kTileK, m_blk * BN, pol_x);
-          bulk_load(sb + C::kABytes + C::kBBytes + C::kRawBytes, sfa + (kb / 2) * 512, 512,
+          bulk_load(sb + C::kABytes + C::kBBytes, a.w + (tile0 + kb) * C::kRawBytes,
+                    C::kRawBytes, &full_bar[stage], pol_w);
+          bulk_load(sb + C::kABytes + C::kBBytes + C::kRawBytes, a.sfa + (tile0 + kb) * 512, 512,
                     &full_bar[stage], pol_w);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sb + C::kABytes + h * C::kBAtomBytes, &tmX, &full_bar[stage],
+                        kb * kTileK + h * kAtomK, m_blk * BN, pol_x);
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -197,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int local = 0;
       constexpr uint32_t idesc = idesc_dense(1, 1, kTileN, BN);
+      const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kABytes), 16, 1024, kSwizzle128B);
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
         int m_blk, n_tile;
         tile_coords(t, a, m_blk, n_tile);
@@ -213,13 +221,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&full_bar[stage], phase, a.status) ||
               !mbar_wait(&conv_bar[stage], phase, a.status)) { abort_flag = 1; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stage_ptr(stage));
-          const uint32_t b_addr = a_addr + C::kABytes;
+          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (C::kStageBytes >> 4);
+          const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (C::kStageBytes >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
-            const uint64_t ad = smem_desc(a_addr + kk * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(b_addr + kk * 32, 16, 1024, kSwizzle128B);
-            mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            // descriptor units (16 B): atom h of the operand, then 32 B per MMA
+            const int h = kk / (kAtomK / kMmaK), off = (kk % (kAtomK / kMmaK)) * 2;
+            mma_f16(d_tmem, ad + h * (C::kAAtomBytes >> 4) + off, bd + h * (C::kBAtomBytes >> 4) + off,
+                    idesc, (kb | kk) != 0);
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -248,24 +257,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           abort_flag = 1; stop = true; break;
         }
         uint8_t* sb = stage_ptr(stage);
-        const uint4* raw = reinterpret_cast<const uint4*>(sb + C::kABytes + C::kBBytes + r * 32);
+        const uint4* raw = reinterpret_cast<const uint4*>(sb + C::kABytes + C::kBBytes + r * 64);
         const uint32_t sfw = *reinterpret_cast<const uint32_t*>(sb + C::kABytes + C::kBBytes +
                                                                C::kRawBytes + sf_off);
-        const int i0 = (kb & 1) * 2;                     // 32-blocks of this stage in the atom
-        const uint32_t s0 = e8m0_bf16x2((sfw >> (8 * i0)) & 0xFF);
-        const uint32_t s1 = e8m0_bf16x2((sfw >> (8 * (i0 + 1))) & 0xFF);
-        uint8_t* dst_row = sb + r * 128;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {                    // 32 elements per half
-          const uint4 q = raw[h];
-          const uint32_t sc = h == 0 ? s0 : s1;
-          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+        for (int q = 0; q < 4; ++q) {                    // 32 elements = one scale block
+          const uint4 v = raw[q];
+          const uint32_t sc = e8m0_bf16x2((sfw >> (8 * q)) & 0xFF);
+          const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+          const int h = q >> 1;                          // swizzle atom (64 elements)
+          uint8_t* dst_row = sb + h * C::kAAtomBytes + r * 128;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {                  // 8 elements -> one 16-byte chunk
             uint32_t o0, o1, o2, o3;
             fp4x4_to_bf16(words[j] & 0xFFFFu, sc, o0, o1);
             fp4x4_to_bf16(words[j] >> 16, sc, o2, o3);
-            const int c = h * 4 + j;                     // chunk index 0..7 in the row
+            const int c = (q & 1) * 4 + j;               // chunk index 0..7 in the atom row
             *reinterpret_cast<uint4*>(dst_row + ((c ^ sw) << 4)) = make_uint4(o0, o1, o2, o3);
           }
         }
@@ -395,25 +402,24 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
 }
 
 template <int BN>
-cudaError_t launch_bn(const CUtensorMap& tw, const CUtensorMap& tx, const Bf16Args& a,
-                      cudaStream_t s) {
+cudaError_t plan_bn(const Bf16Args& a, int num_sms, GemmPlan* plan) {
   using C = Cfg16<BN>;
-  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN>),
-                                     C::kSmem);
+  static_assert(sizeof(Bf16Args) <= sizeof(plan->args), "argument block");
+  const void* fn = reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN>);
+  cudaError_t err = ensure_smem_attr(fn, C::kSmem);
   if (err != cudaSuccess) return err;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int tiles = a.num_blocks * a.n_tiles;
-  const int grid = tiles < sms ? tiles : sms;
-  if (grid <= 0) return cudaSuccess;
-  moe_gemm_bf16w4_kernel<BN><<<grid, kThreads, C::kSmem, s>>>(tw, tx, a);
-  return cudaGetLastError();
+  plan->kernel = fn;
+  plan->grid = tiles < num_sms ? tiles : num_sms;
+  plan->threads = kThreads;
+  plan->smem = C::kSmem;
+  memcpy(plan->args, &a, sizeof(a));
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_bf16w4(int stage, const GemmArgs& g, cudaStream_t s) {
+cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   Bf16Args a{};
   a.stage = stage;
   a.M = g.M; a.topk = g.topk; a.H = g.H; a.Ip = g.Ip; a.E = g.E;
@@ -424,26 +430,28 @@ cudaError_t launch_gemm_bf16w4(int stage, const GemmArgs& g, cudaStream_t s) {
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
   a.num_padded = g.num_padded;
   a.sfa = stage == 1 ? g.w1s : g.w2s;
+  a.w = stage == 1 ? g.w1 : g.w2;
   a.inter = static_cast<__nv_bfloat16*>(g.inter);
   a.acc = g.acc;
   a.status = g.status;
+  plan->grid = 0;
   if (a.num_blocks == 0) return cudaSuccess;
-  CUtensorMap tw, tx;
-  const uint8_t* w = stage == 1 ? g.w1 : g.w2;
   const void* xb = stage == 1 ? g.act : g.inter;
-  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, a.K / 2,
-                 static_cast<uint64_t>(a.E) * a.N, a.K / 2, kTileK / 2, kTileN,
-                 CU_TENSOR_MAP_SWIZZLE_NONE))
+  CUtensorMap* tw = reinterpret_cast<CUtensorMap*>(plan->tmap_a);
+  CUtensorMap* tx = reinterpret_cast<CUtensorMap*>(plan->tmap_b);
+  memset(tw, 0, sizeof(CUtensorMap));   // weights arrive by bulk copy; no tensor map needed
+  if (!encode_2d(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a.K, static_cast<uint64_t>(g.p_max),
+                 static_cast<uint64_t>(a.K) * 2, kAtomK, g.bm, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a.K, static_cast<uint64_t>(g.p_max),
-                 static_cast<uint64_t>(a.K) * 2, kTileK, g.bm, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   switch (g.bm) {
-    case 16: return launch_bn<16>(tw, tx, a, s);
-    case 32: return launch_bn<32>(tw, tx, a, s);
-    case 64: return launch_bn<64>(tw, tx, a, s);
-    case 128: return launch_bn<128>(tw, tx, a, s);
-    case 256: return launch_bn<256>(tw, tx, a, s);
+    case 16: return plan_bn<16>(a, sms, plan);
+    case 32: return plan_bn<32>(a, sms, plan);
+    case 64: return plan_bn<64>(a, sms, plan);
+    case 128: return plan_bn<128>(a, sms, plan);
+    case 256: return plan_bn<256>(a, sms, plan);
   }
   return cudaErrorInvalidValue;
 }

@@ -14,9 +14,11 @@
 // a few routes costs an N=16 MMA instead of a mostly empty 128-row tile.
 //
 // Operand formats in shared memory (128-byte swizzled, K-major):
-//   A  E2M1, expanded by TMA (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B) to 16-byte
+//   A  E2M1, prepacked in HBM as contiguous 8 KB tiles (128 rows x 64 bytes),
+//      expanded by TMA (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B) to 16-byte
 //      units holding 16 codes in their low 8 bytes, i.e. one byte slot per
-//      element as kind::mxf8f6f4 expects for 4-bit operands;
+//      element as kind::mxf8f6f4 expects for 4-bit operands; contiguous rows
+//      stream at ~6 TB/s where 2560-byte-strided 64-byte rows reach ~4 TB/s;
 //   B  E4M3 bytes.
 // Scales: 512-byte atoms (128 rows x four 32-blocks, see sf_atom_off) copied
 // to TMEM with tcgen05.cp .32x128b.warpx4 (4 columns per atom); the MMA for
@@ -28,6 +30,7 @@
 // walks the same sequence and skips tiles past the device-side route count,
 // so launch shapes depend only on host-known sizes (graph capturable).
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include "common.cuh"
@@ -36,6 +39,19 @@
 
 namespace moe {
 namespace {
+
+#ifdef MOE_WAIT_STATS
+// Experiment builds only: per-CTA cycles each role spent waiting on its
+// barriers ([0] producer/empty, [1] MMA/full, [2] MMA/acc_empty,
+// [3] epilogue/acc_full, [4] kernel cycles, [5] epilogue busy cycles).
+__device__ long long g_wait_stats[512][16];   // [cta][(stage-1)*8 + slot]
+#define WAIT_T0() const long long _wt0 = clock64()
+#define WAIT_ADD(i) atomicAdd(reinterpret_cast<unsigned long long*>(&g_wait_stats[blockIdx.x][(a.stage - 1) * 8 + (i)]), \
+                              static_cast<unsigned long long>(clock64() - _wt0))
+#else
+#define WAIT_T0()
+#define WAIT_ADD(i)
+#endif
 
 constexpr int kThreads = 192;
 constexpr int kTileN = 128;    // weight rows per tile (MMA M)
@@ -52,6 +68,7 @@ struct MxArgs {
   const float* sorted_w;
   const int32_t* block_expert;
   const int32_t* num_padded;
+  const uint8_t* w_base; // prepacked weight tiles [E][N/128][K/128][128][64 B]
   const uint8_t* sfa;    // weight scale atoms [E][N/128][K/128][512]
   const uint8_t* sfb;    // route scale atoms [blocks][K/128][na][512]
   uint8_t* inter;        // stage 1 out: E4M3 [p_max, Ip]
@@ -67,19 +84,50 @@ struct Cfg {
   static constexpr int kBBytes = BN * kTileK;
   static constexpr int kSfBytes = 512 * (1 + kNa);
   static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN <= 32 ? 8 : (BN <= 64 ? 7 : (BN <= 128 ? 5 : 4));
+  // Up to block_m 64 two CTAs share an SM (two MMA-issuing threads: at small
+  // N one thread cannot issue tcgen05 work fast enough to keep up with HBM),
+  // so ring, accumulators and scale columns are sized for half an SM.
+  static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
+  static constexpr int kStages = BN <= 16 ? 5 : BN <= 32 ? 4 : (BN <= 64 ? 4 : (BN <= 128 ? 6 : 4));
   static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
+  // Independent accumulators per tile: MMA kk of a k-block adds into
+  // accumulator kk % kSplit, so small-N MMAs do not form one dependent chain;
+  // the epilogue sums them.
+  static constexpr int kSplit = BN <= 16 ? 2 : 1;
+  static constexpr int kAccCols = BN * kSplit;
   static constexpr int kSfCols = 4 * (1 + kNa);                // TMEM columns per stage
-  static constexpr int kColsNeeded = kAccBufs * BN + kStages * kSfCols;
+  static constexpr int kColsNeeded = kAccBufs * kAccCols + kStages * kSfCols;
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64
                                    : kColsNeeded <= 128 ? 128 : kColsNeeded <= 256 ? 256 : 512;
-  static constexpr int kEpiFloats = 32 * (64 + 4);             // stage-1 transpose tile
+  static constexpr int kEpiFloats = 32 * (64 + 4);             // stage-1 / stage-2 transpose tile
   static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStageBytes + kEpiFloats * 4 + 256;
   // TMA transaction bytes of one stage: FP4 A counts packed bytes
   static constexpr uint32_t kTxBytes = kTileN * kTileK / 2 + kBBytes + kSfBytes;
-  static_assert(kColsNeeded <= 512, "TMEM budget");
-  static_assert(kSmem <= 227 * 1024, "smem budget");
+  static_assert(kColsNeeded <= 512 / kCtasPerSm, "TMEM budget");
+  // per SM: 228 KB of shared memory, of which 1 KB is reserved per CTA
+  static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
 };
+
+// Position of the producer (or its L2-prefetch look-ahead) in this CTA's
+// sequence of (tile, k-block) pairs.
+struct Cursor {
+  int t, kb, m_blk, n_tile, e;
+  bool valid;
+};
+
+__device__ __forceinline__ void tile_coords(int t, const struct MxArgs& a, int& m_blk, int& n_tile);
+
+// Moves c to the first tile at or after c.t (stride gridDim.x) that holds routes.
+__device__ __forceinline__ void seek_valid(Cursor& c, const MxArgs& a, int total_tiles, int P,
+                                           int bn) {
+  for (; c.t < total_tiles; c.t += gridDim.x) {
+    tile_coords(c.t, a, c.m_blk, c.n_tile);
+    if (c.m_blk * bn >= P) continue;
+    c.e = __ldg(a.block_expert + c.m_blk);
+    if (c.e >= 0 && c.e < a.E) { c.valid = true; return; }
+  }
+  c.valid = false;
+}
 
 __device__ __forceinline__ void tile_coords(int t, const MxArgs& a, int& m_blk, int& n_tile) {
   if (a.stage == 1) {  // route-block major: the n-tiles of a block share its activations
@@ -92,7 +140,7 @@ __device__ __forceinline__ void tile_coords(int t, const MxArgs& a, int& m_blk, 
 }
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const MxArgs a) {
   using C = Cfg<BN>;
@@ -111,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int P = *a.num_padded;
   const int total_tiles = a.num_blocks * a.n_tiles;
   const int kblocks = a.K / kTileK;
+#ifdef MOE_WAIT_STATS
+  const long long _k0 = clock64();
+#endif
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -135,42 +186,92 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t sf_col0 = C::kAccBufs * BN;
+  const uint32_t sf_col0 = C::kAccBufs * C::kAccCols;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Per tile the weight tiles (prepacked: consecutive k-blocks are
+    // consecutive 8 KB blocks), both scale arrays and the route rows advance
+    // by constant steps. A second cursor runs kPrefetch k-blocks ahead
+    // (across tiles) and prefetches weight tiles into L2, so the loads that
+    // fill the shared-memory ring mostly hit L2.
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_x = policy_evict_last();    // routes: reused across n-tiles
+      constexpr int kPrefetch = 16;
+      constexpr uint32_t kWTile = kTileN * kTileK / 2;   // 8 KB
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
-        int m_blk, n_tile;
-        tile_coords(t, a, m_blk, n_tile);
-        if (m_blk * BN >= P) continue;
-        const int e = __ldg(a.block_expert + m_blk);
-        if (e < 0 || e >= a.E) continue;
-        const int row_a = e * a.N + n_tile * kTileN;
-        const uint8_t* sfa = a.sfa + ((static_cast<int64_t>(e) * a.n_tiles + n_tile) * kblocks) * 512;
-        const uint8_t* sfb = a.sfb + static_cast<int64_t>(m_blk) * kblocks * C::kNa * 512;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
-          uint8_t* sbase = stages + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-          tma_load_2d(sbase, &tmA, &full_bar[stage], kb * kTileK, row_a, pol_w);
-          tma_load_2d(sbase + C::kABytes, &tmB, &full_bar[stage], kb * kTileK, m_blk * BN, pol_x);
-          bulk_load(sbase + C::kABytes + C::kBBytes, sfa + kb * 512, 512, &full_bar[stage], pol_w);
-          bulk_load(sbase + C::kABytes + C::kBBytes + 512, sfb + kb * C::kNa * 512,
-                    512 * C::kNa, &full_bar[stage], pol_x);
-          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+      uint8_t* sbase = stages;
+      Cursor cur{static_cast<int>(blockIdx.x), 0, 0, 0, 0, false};
+      seek_valid(cur, a, total_tiles, P, BN);
+      Cursor pf = cur;
+      const uint8_t* pf_w = nullptr;
+      auto pf_tile = [&]() {
+        pf_w = a.w_base + (static_cast<int64_t>(pf.e) * a.n_tiles + pf.n_tile) * kblocks * kWTile;
+      };
+      if (pf.valid) pf_tile();
+      auto pf_step = [&]() {
+        if (!pf.valid) return;
+        bulk_prefetch_l2(pf_w + static_cast<int64_t>(pf.kb) * kWTile, kWTile);
+        if (++pf.kb == kblocks) {
+          pf.kb = 0;
+          pf.t += gridDim.x;
+          seek_valid(pf, a, total_tiles, P, BN);
+          if (pf.valid) pf_tile();
         }
+      };
+      for (int i = 0; i < kPrefetch; ++i) pf_step();
+      while (cur.valid && !abort_flag) {
+        const int64_t wtile = static_cast<int64_t>(cur.e) * a.n_tiles + cur.n_tile;
+        int row_a = static_cast<int>(wtile * kblocks * kTileN);
+        const uint8_t* sfa = a.sfa + wtile * kblocks * 512;
+        const uint8_t* sfb = a.sfb + static_cast<int64_t>(cur.m_blk) * kblocks * C::kNa * 512;
+        const int row_b = cur.m_blk * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          {
+            WAIT_T0();
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
+            WAIT_ADD(0);
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+          tma_load_2d(sbase, &tmA, &full_bar[stage], 0, row_a, pol_w);
+          tma_load_2d(sbase + C::kABytes, &tmB, &full_bar[stage], kb * kTileK, row_b, pol_x);
+          bulk_load(sbase + C::kABytes + C::kBBytes, sfa, 512, &full_bar[stage], pol_w);
+          bulk_load(sbase + C::kABytes + C::kBBytes + 512, sfb, 512 * C::kNa, &full_bar[stage],
+                    pol_x);
+          pf_step();
+          row_a += kTileN;
+          sfa += 512;
+          sfb += 512 * C::kNa;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+            sbase = stages;
+          } else {
+            sbase += C::kStageBytes;
+          }
+        }
+        cur.t += gridDim.x;
+        seek_valid(cur, a, total_tiles, P, BN);
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
+    // At small N the tensor core is far faster than one thread can issue, so
+    // this loop is kept minimal: descriptors are built once and advanced by
+    // adding to their 14-bit start-address field (address >> 4), instruction
+    // descriptors are compile-time constants.
     if (lane == 0) {
+      const uint64_t a_desc0 = smem_desc(smem_u32(stages), 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(smem_u32(stages + C::kABytes), 16, 1024, kSwizzle128B);
+      const uint64_t sf_desc0 = smem_desc(smem_u32(stages + C::kABytes + C::kBBytes), 0, 128,
+                                          kSwizzleNone);
+      constexpr uint32_t kStageStep = C::kStageBytes >> 4;   // descriptor units per stage
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t sdesc_off = 0;                                // stage * kStageStep
+      uint32_t sf_tmem = tmem + sf_col0;                      // this stage's scale columns
       int local = 0;
       for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
         int m_blk, n_tile;
@@ -181,32 +282,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
         ++local;
-        if (!mbar_wait(&acc_empty[ab], acc_phase ^ 1, a.status)) { abort_flag = 1; break; }
+        {
+          WAIT_T0();
+          if (!mbar_wait(&acc_empty[ab], acc_phase ^ 1, a.status)) { abort_flag = 1; break; }
+          WAIT_ADD(2);
+        }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + ab * BN;
+        const uint32_t d_tmem = tmem + ab * C::kAccCols;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, a.status)) { abort_flag = 1; break; }
-          tc_fence_after();
-          uint8_t* sbase = stages + stage * C::kStageBytes;
-          const uint32_t a_addr = smem_u32(sbase);
-          const uint32_t b_addr = smem_u32(sbase + C::kABytes);
-          const uint32_t sf_addr = smem_u32(sbase + C::kABytes + C::kBBytes);
-          const uint32_t sfa_t = tmem + sf_col0 + stage * C::kSfCols;
-          const uint32_t sfb_t = sfa_t + 4;
-          tmem_cp_32x128b_warpx4(sfa_t, smem_desc(sf_addr, 0, 128, kSwizzleNone));
+          {
+            WAIT_T0();
+            if (!mbar_wait(&full_bar[stage], phase, a.status)) { abort_flag = 1; break; }
+            WAIT_ADD(1);
+          }
+          tmem_cp_32x128b_warpx4(sf_tmem, sf_desc0 + sdesc_off);
 #pragma unroll
           for (int j = 0; j < C::kNa; ++j)
-            tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
-                                   smem_desc(sf_addr + 512 * (1 + j), 0, 128, kSwizzleNone));
+            tmem_cp_32x128b_warpx4(sf_tmem + 4 + 4 * j, sf_desc0 + sdesc_off + 32 * (1 + j));
+          const uint64_t ad = a_desc0 + sdesc_off;
+          const uint64_t bd = b_desc0 + sdesc_off;
 #pragma unroll
           for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
-            const uint64_t ad = smem_desc(a_addr + kk * kMmaK, 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(b_addr + kk * kMmaK, 16, 1024, kSwizzle128B);
-            mma_mxf8f6f4(d_tmem, ad, bd, idesc_mx(5, 0, kTileN, BN, kk, kk), sfa_t, sfb_t,
-                         (kb | kk) != 0);
+            mma_mxf8f6f4(d_tmem + (kk % C::kSplit) * BN, ad + 2 * kk, bd + 2 * kk,
+                         idesc_mx(5, 0, kTileN, BN, kk, kk), sf_tmem, sf_tmem + 4,
+                         kb > 0 || kk >= C::kSplit);
           }
           tc_commit(&empty_bar[stage]);
-          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+            sdesc_off = 0;
+            sf_tmem = tmem + sf_col0;
+          } else {
+            sdesc_off += kStageStep;
+            sf_tmem += C::kSfCols;
+          }
         }
         tc_commit(&acc_full[ab]);
       }
@@ -230,26 +340,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ab = local % C::kAccBufs;
       const uint32_t acc_phase = (local / C::kAccBufs) & 1;
       ++local;
-      if (abort_flag || !mbar_wait(&acc_full[ab], acc_phase, a.status)) { abort_flag = 1; break; }
+      {
+        WAIT_T0();
+        if (abort_flag || !mbar_wait(&acc_full[ab], acc_phase, a.status)) { abort_flag = 1; break; }
+        if (threadIdx.x == 64) WAIT_ADD(3);
+      }
+#ifdef MOE_WAIT_STATS
+      const long long _busy0 = clock64();
+#endif
       tc_fence_after();
-      const uint32_t d_tmem = tmem + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t d_tmem = tmem + ab * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
       constexpr int kChunk = BN < 32 ? BN : 32;
       for (int c0 = 0; c0 < BN; c0 += kChunk) {
         float v[32];
-        {
+#pragma unroll
+        for (int sp = 0; sp < C::kSplit; ++sp) {
           uint32_t r[32];
           if constexpr (kChunk == 32) {
-            tmem_ld_32x32b_x32(d_tmem + c0, r);
+            tmem_ld_32x32b_x32(d_tmem + sp * BN + c0, r);
           } else {
             uint32_t r16[16];
-            tmem_ld_32x32b_x16(d_tmem + c0, r16);
+            tmem_ld_32x32b_x16(d_tmem + sp * BN + c0, r16);
 #pragma unroll
             for (int i = 0; i < 16; ++i) r[i] = r16[i];
           }
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r[i]);
+          for (int i = 0; i < kChunk; ++i)
+            v[i] = sp == 0 ? __uint_as_float(r[i]) : v[i] + __uint_as_float(r[i]);
         }
         if (a.stage == 1) {
           // gate (even row) / up (odd row) pairs sit in adjacent lanes
@@ -305,26 +424,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          // route info of this chunk's columns, one per lane, broadcast by shuffle
-          int tok = -1;
-          float wgt = 0.f;
-          if (lane < kChunk) {
-            const int64_t p = p_base + c0 + lane;
-            const int r = __ldg(a.sorted_route + p);
-            if (r < R) { tok = r / a.topk; wgt = __ldg(a.sorted_w + p); }
-          }
-          const int n = n_tile * kTileN + row;
+          // stage 2: transpose the chunk through shared memory so that each
+          // thread owns 4 consecutive features of one route and adds them
+          // with one 16-byte reduction (a warp covers 512 contiguous bytes)
+          for (int h = 0; h < kChunk; h += 16) {
+            named_bar_sync(1, 128);
 #pragma unroll
-          for (int i = 0; i < kChunk; ++i) {
-            const int ti = __shfl_sync(0xffffffffu, tok, i);
-            const float wi = __shfl_sync(0xffffffffu, wgt, i);
-            if (ti >= 0) atomicAdd(a.acc + static_cast<int64_t>(ti) * a.H + n, wi * v[i]);
+            for (int i = 0; i < 16; ++i)
+              if (h + i < kChunk) epi[i * 132 + row] = v[h + i];
+            named_bar_sync(1, 128);
+            const int g = et & 31, cb = et >> 5;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = cb + 4 * j;
+              if (h + c >= kChunk) continue;
+              const int64_t p = p_base + c0 + h + c;
+              const int rr = __ldg(a.sorted_route + p);
+              if (rr >= R) continue;
+              const float wgt = __ldg(a.sorted_w + p);
+              float4 f = *reinterpret_cast<const float4*>(epi + c * 132 + 4 * g);
+              f.x *= wgt; f.y *= wgt; f.z *= wgt; f.w *= wgt;
+              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(rr / a.topk) * a.H +
+                                                  n_tile * kTileN + 4 * g),
+                        f);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
+#ifdef MOE_WAIT_STATS
+      if (threadIdx.x == 64)
+        atomicAdd(reinterpret_cast<unsigned long long*>(&g_wait_stats[blockIdx.x][(a.stage - 1) * 8 + 5]),
+                  static_cast<unsigned long long>(clock64() - _busy0));
+#endif
     }
   }
   tc_fence_before();
@@ -333,7 +467,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+#ifdef MOE_WAIT_STATS
+  if (threadIdx.x == 0)
+    atomicAdd(reinterpret_cast<unsigned long long*>(&g_wait_stats[blockIdx.x][(a.stage - 1) * 8 + 4]),
+              static_cast<unsigned long long>(clock64() - _k0));
+#endif
 }
+
+}  // namespace
+
+#ifdef MOE_WAIT_STATS
+extern "C" void moe_debug_wait_stats(long long* host_out, int reset) {
+  cudaMemcpyFromSymbol(host_out, g_wait_stats, sizeof(g_wait_stats));
+  if (reset) {
+    static long long zeros[512][16] = {};
+    cudaMemcpyToSymbol(g_wait_stats, zeros, sizeof(zeros));
+  }
+}
+#endif
+
+namespace {
 
 // ---------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -363,17 +516,20 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
 }
 
 template <int BN>
-cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const MxArgs& a,
-                      int num_sms, cudaStream_t s) {
+cudaError_t plan_bn(const MxArgs& a, int num_sms, GemmPlan* plan) {
   using C = Cfg<BN>;
-  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN>),
-                                     C::kSmem);
+  static_assert(sizeof(MxArgs) <= sizeof(plan->args), "argument block");
+  const void* fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN>);
+  cudaError_t err = ensure_smem_attr(fn, C::kSmem);
   if (err != cudaSuccess) return err;
   const int tiles = a.num_blocks * a.n_tiles;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  if (grid <= 0) return cudaSuccess;
-  moe_gemm_mx_kernel<BN><<<grid, kThreads, C::kSmem, s>>>(ta, tb, a);
-  return cudaGetLastError();
+  const int slots = num_sms * C::kCtasPerSm;
+  plan->kernel = fn;
+  plan->grid = tiles < slots ? tiles : slots;
+  plan->threads = kThreads;
+  plan->smem = C::kSmem;
+  memcpy(plan->args, &a, sizeof(a));
+  return cudaSuccess;
 }
 
 int sm_count() {
@@ -385,7 +541,7 @@ int sm_count() {
 
 }  // namespace
 
-cudaError_t launch_gemm_mx(int stage, const GemmArgs& g, cudaStream_t s) {
+cudaError_t prepare_gemm_mx(int stage, const GemmArgs& g, GemmPlan* plan) {
   MxArgs a{};
   a.stage = stage;
   a.M = g.M; a.topk = g.topk; a.H = g.H; a.Ip = g.Ip; a.E = g.E;
@@ -396,31 +552,45 @@ cudaError_t launch_gemm_mx(int stage, const GemmArgs& g, cudaStream_t s) {
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
   a.num_padded = g.num_padded;
   a.sfa = stage == 1 ? g.w1s : g.w2s;
+  a.w_base = stage == 1 ? g.w1 : g.w2;
   a.sfb = stage == 1 ? g.act_sf : g.inter_sf;
   a.inter = static_cast<uint8_t*>(g.inter);
   a.inter_sf = g.inter_sf;
   a.acc = g.acc;
   a.status = g.status;
+  plan->grid = 0;
   if (a.num_blocks == 0) return cudaSuccess;
-
-  CUtensorMap ta, tb;
   const uint8_t* w = stage == 1 ? g.w1 : g.w2;
   const void* xb = stage == 1 ? g.act : g.inter;
-  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, a.K,
-                 static_cast<uint64_t>(a.E) * a.N, a.K / 2, 128, kTileN))
+  CUtensorMap* ta = reinterpret_cast<CUtensorMap*>(plan->tmap_a);
+  CUtensorMap* tb = reinterpret_cast<CUtensorMap*>(plan->tmap_b);
+  if (!encode_2d(ta, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w, kTileK,
+                 static_cast<uint64_t>(a.E) * a.N * (a.K / kTileK), kTileK / 2, kTileK, kTileN))
     return cudaErrorInvalidValue;
-  if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xb, a.K, static_cast<uint64_t>(g.p_max), a.K,
+  if (!encode_2d(tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, xb, a.K, static_cast<uint64_t>(g.p_max), a.K,
                  128, g.bm))
     return cudaErrorInvalidValue;
   const int sms = sm_count();
   switch (g.bm) {
-    case 16: return launch_bn<16>(ta, tb, a, sms, s);
-    case 32: return launch_bn<32>(ta, tb, a, sms, s);
-    case 64: return launch_bn<64>(ta, tb, a, sms, s);
-    case 128: return launch_bn<128>(ta, tb, a, sms, s);
-    case 256: return launch_bn<256>(ta, tb, a, sms, s);
+    case 16: return plan_bn<16>(a, sms, plan);
+    case 32: return plan_bn<32>(a, sms, plan);
+    case 64: return plan_bn<64>(a, sms, plan);
+    case 128: return plan_bn<128>(a, sms, plan);
+    case 256: return plan_bn<256>(a, sms, plan);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t s) {
+  if (plan.grid <= 0) return cudaSuccess;
+  void* args[3] = {const_cast<unsigned char*>(plan.tmap_a), const_cast<unsigned char*>(plan.tmap_b),
+                   const_cast<unsigned char*>(plan.args)};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(plan.threads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = s;
+  return cudaLaunchKernelExC(&cfg, plan.kernel, args);
 }
 
 }  // namespace moe

@@ -10,25 +10,27 @@ namespace moe {
 // Sets the dynamic shared-memory limit of `func` once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes);
 
-size_t sort_smem_bytes(int E);
+int sort_num_ctas(int R);
+size_t sort_scratch_bytes(int R, int E);
 cudaError_t launch_sort(const int32_t* ids, const float* wts, int R, int E, int bm, int64_t p_max,
                         int32_t* sorted_route, float* sorted_w, int32_t* block_expert,
                         int32_t* expert_off, int32_t* num_padded, int32_t* route_pos,
-                        int32_t* status, cudaStream_t s);
+                        int32_t* status, int32_t* scratch, cudaStream_t s);
 
 cudaError_t launch_quant_act(const void* x, int M, int K, int ldx, uint8_t* q, uint8_t* scale,
                              cudaStream_t s);
 
+cudaError_t launch_prepack_weights(const uint8_t* w, int E, int N, int K, uint8_t* out,
+                                   cudaStream_t s);
 cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uint8_t* out,
                                   cudaStream_t s);
 
-// Gathers the activation rows of the sorted routes (quantised to FP8 with
-// scale atoms for a8w4, copied as BF16 for a16w4), zeroes pad rows, and
+// Writes each token's activation row to the sorted position of each of its
+// routes (quantised to FP8 with scale atoms for a8w4, as BF16 for a16w4) and
 // zeroes the FP32 accumulator [M, H].
 cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, int bm,
-                              int64_t p_max, const int32_t* sorted_route,
-                              const int32_t* num_padded, void* act, uint8_t* act_sf,
-                              float* acc, cudaStream_t s);
+                              const int32_t* route_pos, void* act, uint8_t* act_sf, float* acc,
+                              cudaStream_t s);
 
 cudaError_t launch_finalize(const float* acc, int64_t n, void* out, cudaStream_t s);
 
@@ -52,10 +54,20 @@ struct GemmArgs {
   int32_t* status;
 };
 
+// A grouped-GEMM launch with all host-side work (tensor-map encoding,
+// attribute setup) done by prepare_*; launch_gemm only enqueues the kernel.
+struct GemmPlan {
+  alignas(64) unsigned char tmap_a[128];   // CUtensorMap of the weights
+  alignas(64) unsigned char tmap_b[128];   // CUtensorMap of the route rows
+  unsigned char args[256];                 // kernel argument block
+  const void* kernel;
+  int grid, threads, smem;
+};
 // tcgen05 block-scaled grouped GEMM, a8w4, stage 1 or 2.
-cudaError_t launch_gemm_mx(int stage, const GemmArgs& a, cudaStream_t s);
+cudaError_t prepare_gemm_mx(int stage, const GemmArgs& a, GemmPlan* plan);
 // tcgen05 BF16 x (MXFP4 dequantised in shared memory) grouped GEMM, a16w4.
-cudaError_t launch_gemm_bf16w4(int stage, const GemmArgs& a, cudaStream_t s);
+cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& a, GemmPlan* plan);
+cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t s);
 
 cudaError_t launch_stage1_simt(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_stage2_simt(const GemmArgs& a, cudaStream_t s);

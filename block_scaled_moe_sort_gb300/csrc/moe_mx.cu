@@ -85,6 +85,7 @@ void build_layout(int M, int H, int Ip, int E, int topk, bool a16, moe_ws_layout
   L->sorted_w_off = take(4 * pm);
   L->block_expert_off = take(4 * nblk);
   L->route_pos_off = take(4 * R);
+  L->sort_scratch_off = take(static_cast<int64_t>(sort_scratch_bytes(static_cast<int>(R), E)));
   L->act_off = take(pm * H * (a16 ? 2 : 1));
   L->act_sf_off = take(a16 ? 0 : nblk * (H / 128) * atoms * 512);
   L->inter_off = take(pm * Ip * (a16 ? 2 : 1));
@@ -155,13 +156,14 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   const int R = M * topk;
 
   prof_mark(0, true, s);
+  int32_t* sort_scratch = reinterpret_cast<int32_t*>(base + L.sort_scratch_off);
   cudaError_t e = launch_sort(ids, wts, R, E, L.block_m, L.p_max, sorted_route, sorted_w,
-                              block_expert, expert_off, num_padded, route_pos, status, s);
+                              block_expert, expert_off, num_padded, route_pos, status,
+                              sort_scratch, s);
   if (e != cudaSuccess) return from_cuda(e);
   prof_mark(0, false, s);
   prof_mark(1, true, s);
-  e = launch_gather_act(a16, x, M, H, topk, L.block_m, L.p_max, sorted_route, num_padded, act,
-                        act_sf, acc, s);
+  e = launch_gather_act(a16, x, M, H, topk, L.block_m, route_pos, act, act_sf, acc, s);
   if (e != cudaSuccess) return from_cuda(e);
   prof_mark(1, false, s);
   GemmArgs g{};
@@ -173,12 +175,17 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   g.w1 = w1; g.w1s = w1s; g.w2 = w2; g.w2s = w2s;
   g.act = act; g.act_sf = act_sf; g.inter = inter; g.inter_sf = inter_sf; g.acc = acc;
   g.status = status;
+  GemmPlan plan1, plan2;
+  e = a16 ? prepare_gemm_bf16w4(1, g, &plan1) : prepare_gemm_mx(1, g, &plan1);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = a16 ? prepare_gemm_bf16w4(2, g, &plan2) : prepare_gemm_mx(2, g, &plan2);
+  if (e != cudaSuccess) return from_cuda(e);
   prof_mark(2, true, s);
-  e = a16 ? launch_gemm_bf16w4(1, g, s) : launch_gemm_mx(1, g, s);
+  e = launch_gemm(plan1, s);
   if (e != cudaSuccess) return from_cuda(e);
   prof_mark(2, false, s);
   prof_mark(3, true, s);
-  e = a16 ? launch_gemm_bf16w4(2, g, s) : launch_gemm_mx(2, g, s);
+  e = launch_gemm(plan2, s);
   if (e != cudaSuccess) return from_cuda(e);
   prof_mark(3, false, s);
   prof_mark(4, true, s);
@@ -214,10 +221,15 @@ int64_t moe_sort_max_padded(int M, int topk, int E, int block_m) {
   return max_padded(static_cast<int64_t>(M) * topk, E, block_m);
 }
 
+size_t moe_sort_workspace_bytes(int M, int topk, int E, int block_m) {
+  if (M < 0 || topk <= 0 || E <= 0 || !valid_bm(block_m)) return 0;
+  return sort_scratch_bytes(M * topk, E);
+}
+
 moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M, int topk, int E,
                       int block_m, int32_t* sorted_route, float* sorted_w, int32_t* block_expert,
-                      int32_t* expert_off, int32_t* num_padded, int32_t* route_pos,
-                      moe_stream_t stream) {
+                      int32_t* expert_off, int32_t* num_padded, int32_t* route_pos, void* ws,
+                      size_t ws_bytes, moe_stream_t stream) {
   if (M < 0 || topk <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
   if (!valid_bm(block_m) || E > kMaxExperts || topk > kMaxTopk) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(M) * topk > (int64_t(1) << 24)) return MOE_ERR_UNSUPPORTED;
@@ -225,9 +237,12 @@ moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M,
   if (!expert_off || !num_padded) return MOE_ERR_INVALID_ARG;
   if (pm > 0 && (!sorted_route || !sorted_w || !block_expert)) return MOE_ERR_INVALID_ARG;
   if (M > 0 && (!topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+  const size_t need = sort_scratch_bytes(M * topk, E);
+  if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  if (ws && !aligned(ws)) return MOE_ERR_ALIGNMENT;
   return from_cuda(launch_sort(topk_ids, topk_weights, M * topk, E, block_m, pm, sorted_route,
                                sorted_w, block_expert, expert_off, num_padded, route_pos, nullptr,
-                               reinterpret_cast<cudaStream_t>(stream)));
+                               static_cast<int32_t*>(ws), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t* q,
@@ -238,6 +253,20 @@ moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t
   if (M > 0 && (!aligned(x_bf16) || !aligned(q) || !aligned(scale))) return MOE_ERR_ALIGNMENT;
   return from_cuda(launch_quant_act(x_bf16, M, K, ldx, q, scale,
                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_prepacked_weight_bytes(int E, int N, int K) {
+  if (E <= 0 || N <= 0 || K <= 0 || N % 128 || K % 128) return 0;
+  return static_cast<size_t>(E) * N * (K / 2);
+}
+
+moe_status_t moe_prepack_weights_mx(const uint8_t* w, int E, int N, int K, uint8_t* out,
+                                    moe_stream_t stream) {
+  if (E <= 0 || N <= 0 || K <= 0 || !w || !out || w == out) return MOE_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(w) || !aligned(out)) return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_prepack_weights(w, E, N, K, out,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_prepacked_scale_bytes(int E, int N, int K) {

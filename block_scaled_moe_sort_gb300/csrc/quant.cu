@@ -54,43 +54,75 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
   }
 }
 
+// One warp per token: the token row is read once (all of a lane's 16-byte
+// loads issued before any use), quantised once (a8w4), and written to the
+// sorted position of each of its routes, scale bytes into the route block's
+// MMA atoms. Rows of pad entries are never written: their GEMM columns are
+// discarded by both epilogues. The CTAs also zero the FP32 accumulator.
 template <bool A16>
 __global__ void __launch_bounds__(256) gather_act_kernel(
-    const __nv_bfloat16* __restrict__ x, int M, int H, int topk, int bm, int64_t p_max,
-    const int32_t* __restrict__ sorted_route, const int32_t* __restrict__ num_padded,
-    void* __restrict__ act, uint8_t* __restrict__ act_sf, float* __restrict__ acc) {
+    const __nv_bfloat16* __restrict__ x, int M, int H, int topk, int bm,
+    const int32_t* __restrict__ route_pos, void* __restrict__ act, uint8_t* __restrict__ act_sf,
+    float* __restrict__ acc) {
+  constexpr int kBatch = 5;                 // 32-blocks per lane held at once
   const int lane = threadIdx.x & 31;
-  const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int P = *num_padded;
-  const int R = M * topk;
-  if (p < P) {
-    const int r = __ldg(sorted_route + p);
-    const bool pad = r >= R;
-    const int t = pad ? 0 : r / topk;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < M) {
+    // route positions of this token, one per lane
+    const int my_pos = lane < topk ? __ldg(route_pos + static_cast<int64_t>(t) * topk + lane) : -1;
     const __nv_bfloat16* xr = x + static_cast<int64_t>(t) * H;
-    if (A16) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(act) + p * H);
-      const uint4* src = reinterpret_cast<const uint4*>(xr);
-      for (int i = lane; i < H / 8; i += 32) dst[i] = pad ? make_uint4(0, 0, 0, 0) : __ldg(src + i);
-    } else {
-      uint8_t* dst = static_cast<uint8_t*>(act) + p * H;
-      const int blk = static_cast<int>(p / bm), rr = static_cast<int>(p % bm);
-      const int atoms = (bm + 127) / 128;
-      const int nslab = H / 128;
-      for (int b = lane; b < H / 32; b += 32) {
-        uint32_t c[8];
-        uint8_t sb = 0;
-        if (pad) {
+    const int nblk = H / 32;
+    const int atoms = (bm + 127) / 128;
+    const int nslab = H / 128;
+    for (int b0 = 0; b0 < nblk; b0 += 32 * kBatch) {
+      uint4 raw[kBatch][4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) c[i] = 0u;
+      for (int i = 0; i < kBatch; ++i) {
+        const int b = b0 + i * 32 + lane;
+        if (b < nblk) {
+          const uint4* src = reinterpret_cast<const uint4*>(xr + b * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) raw[i][q] = __ldg(src + q);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int b = b0 + i * 32 + lane;
+        const bool in = b < nblk;
+        if (A16) {
+          for (int j = 0; j < topk; ++j) {
+            const int p = __shfl_sync(0xffffffffu, my_pos, j);
+            if (p < 0 || !in) continue;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(act) +
+                                                  static_cast<int64_t>(p) * H + b * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = raw[i][q];
+          }
         } else {
           float v[32];
-          load_bf16x32(xr + b * 32, v);
-          sb = quant_block32(v, c);
+          uint32_t c[8];
+          uint8_t sb = 0;
+          if (in) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t w4[4] = {raw[i][q].x, raw[i][q].y, raw[i][q].z, raw[i][q].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                v[q * 8 + 2 * j] = __uint_as_float(w4[j] << 16);
+                v[q * 8 + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+              }
+            }
+            sb = quant_block32(v, c);
+          }
+          for (int j = 0; j < topk; ++j) {
+            const int p = __shfl_sync(0xffffffffu, my_pos, j);
+            if (p < 0 || !in) continue;
+            store_codes32(static_cast<uint8_t*>(act) + static_cast<int64_t>(p) * H + b * 32, c);
+            const int blk = p / bm, rr = p % bm;
+            const int64_t atom = (static_cast<int64_t>(blk) * nslab + b / 4) * atoms + rr / 128;
+            act_sf[atom * 512 + sf_atom_off(rr & 127, b & 3)] = sb;
+          }
         }
-        store_codes32(dst + b * 32, c);
-        const int64_t atom = (static_cast<int64_t>(blk) * nslab + b / 4) * atoms + rr / 128;
-        act_sf[atom * 512 + sf_atom_off(rr & 127, b & 3)] = sb;
       }
     }
   }
@@ -118,6 +150,28 @@ __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* __re
     const int r = (off >> 4) + 32 * ((off & 15) >> 2);
     const int i = off & 3;
     out[o] = scale[(static_cast<int64_t>(e) * N + nb * 128 + r) * (K / 32) + kb * 4 + i];
+  }
+}
+
+// Row-major packed codes [E][N][K/2] -> tiles [E][N/128][K/128][128][64 B],
+// one 16-byte chunk per thread.
+__global__ void __launch_bounds__(256) prepack_weights_kernel(const uint8_t* __restrict__ w,
+                                                              int E, int N, int K,
+                                                              uint8_t* __restrict__ out) {
+  const int64_t total = static_cast<int64_t>(E) * N * (K / 2) / 16;
+  const int nb_n = N / 128, nb_k = K / 128;
+  for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
+       o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(o & 3);          // 16-byte chunk within the 64-byte row piece
+    int64_t a = o >> 2;
+    const int r = static_cast<int>(a & 127);
+    a >>= 7;
+    const int kb = static_cast<int>(a % nb_k);
+    a /= nb_k;
+    const int nb = static_cast<int>(a % nb_n);
+    const int e = static_cast<int>(a / nb_n);
+    const int64_t src = (static_cast<int64_t>(e) * N + nb * 128 + r) * (K / 2) + kb * 64 + c * 16;
+    reinterpret_cast<uint4*>(out)[o] = *reinterpret_cast<const uint4*>(w + src);
   }
 }
 
@@ -156,17 +210,16 @@ cudaError_t launch_quant_act(const void* x, int M, int K, int ldx, uint8_t* q, u
 }
 
 cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, int bm,
-                              int64_t p_max, const int32_t* sorted_route,
-                              const int32_t* num_padded, void* act, uint8_t* act_sf,
-                              float* acc, cudaStream_t s) {
-  const int grid = static_cast<int>((p_max + 7) / 8) > 0 ? static_cast<int>((p_max + 7) / 8) : 1;
+                              const int32_t* route_pos, void* act, uint8_t* act_sf, float* acc,
+                              cudaStream_t s) {
+  if (topk > 32) return cudaErrorInvalidValue;
+  const int grid = (M + 7) / 8 > 0 ? (M + 7) / 8 : 1;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (a16)
-    gather_act_kernel<true><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, p_max, sorted_route,
-                                                 num_padded, act, act_sf, acc);
+    gather_act_kernel<true><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, route_pos, act, act_sf, acc);
   else
-    gather_act_kernel<false><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, p_max, sorted_route,
-                                                  num_padded, act, act_sf, acc);
+    gather_act_kernel<false><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, route_pos, act, act_sf,
+                                                  acc);
   return cudaGetLastError();
 }
 
@@ -175,6 +228,14 @@ cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uin
   const int64_t total = static_cast<int64_t>(E) * N * (K / 32);
   if (total == 0) return cudaSuccess;
   prepack_scales_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, s>>>(scale, E, N, K, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepack_weights(const uint8_t* w, int E, int N, int K, uint8_t* out,
+                                   cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(E) * N * (K / 2) / 16;
+  if (total == 0) return cudaSuccess;
+  prepack_weights_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, s>>>(w, E, N, K, out);
   return cudaGetLastError();
 }
 

@@ -80,16 +80,21 @@ const char* moe_status_string(moe_status_t s);
  *   num_padded   [1]     int32  P = sum_e ceil(cnt_e/block_m)*block_m
  *   route_pos    [M*topk] int32 sorted position of r, -1 if dropped
  *                (may be NULL)
+ * ws/ws_bytes: scratch of at least moe_sort_workspace_bytes (may be NULL when
+ * that is 0); MOE_ERR_WORKSPACE if too small.
  * Positions in [P, P_max) are filled with the pad sentinel. When P_max is 0
  * (M == 0) the three P_max-sized outputs may be NULL.
  * Limits: 1 <= E <= 512, 1 <= topk <= 16, block_m in {16,32,64,128,256},
  * M*topk <= 2^24. M == 0 is allowed (writes the empty result).
  */
 int64_t moe_sort_max_padded(int M, int topk, int E, int block_m);
+/* Scratch the sort needs (device, caller-allocated): 0 up to 8192 routes,
+ * else 4*E bytes per 8192 routes (per-CTA expert histograms). */
+size_t moe_sort_workspace_bytes(int M, int topk, int E, int block_m);
 moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M, int topk,
                       int E, int block_m, int32_t* sorted_route, float* sorted_w,
                       int32_t* block_expert, int32_t* expert_off, int32_t* num_padded,
-                      int32_t* route_pos, moe_stream_t stream);
+                      int32_t* route_pos, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* -------------------------------------------------------- activation quant
  * moe_quant_act_mx: x BF16 [M, K] (row stride ldx elements) -> q E4M3 codes
@@ -101,6 +106,19 @@ moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M,
  */
 moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t* q,
                               uint8_t* scale, moe_stream_t stream);
+
+/* --------------------------------------------------------- weight prepack
+ * The GEMMs stream each 128-row x 128-K weight tile as one contiguous 8 KB
+ * block (one TMA request per tile instead of 128 strided 64-byte rows).
+ * moe_prepack_weights_mx converts row-major packed E2M1 codes [E, N, K/2]
+ * into [E][N/128][K/128][128 rows][64 bytes]: tile (nb, kb) of expert e holds
+ * rows nb*128 .. nb*128+127, bytes kb*64 .. kb*64+63 of each row, rows in
+ * order. Call once at weight-load time; the output is what fused_moe_* take
+ * as w1 / w2. Limits: N % 128 == 0, K % 128 == 0; out must not alias w.
+ */
+size_t moe_prepacked_weight_bytes(int E, int N, int K);
+moe_status_t moe_prepack_weights_mx(const uint8_t* w, int E, int N, int K, uint8_t* out,
+                                    moe_stream_t stream);
 
 /* ---------------------------------------------------- weight scale prepack
  * The GEMMs read weight scales in 512-byte atoms. moe_prepack_scales_mx
@@ -131,7 +149,9 @@ typedef struct {
   int64_t sorted_w_off;     /* float [p_max] */
   int64_t block_expert_off; /* int32 [p_max/block_m] */
   int64_t route_pos_off;    /* int32 [M*topk] */
-  int64_t act_off;       /* a8w4: E4M3 [p_max, H] gathered rows; a16w4: BF16 [p_max, H] */
+  int64_t sort_scratch_off; /* int32 per-CTA expert histograms of the sort */
+  int64_t act_off;       /* a8w4: E4M3 [p_max, H] route rows; a16w4: BF16 [p_max, H];
+                            rows of pad entries are not written */
   int64_t act_sf_off;    /* a8w4: scale atoms [p_max/block_m][H/128][ceil(block_m/128)][512] */
   int64_t inter_off;     /* a8w4: E4M3 [p_max, Ip]; a16w4: BF16 [p_max, Ip] */
   int64_t inter_sf_off;  /* a8w4: scale atoms [p_max/block_m][Ip/128][ceil(block_m/128)][512] */
@@ -147,10 +167,11 @@ moe_status_t fused_moe_workspace_layout(int M, int H, int Ip, int E, int topk, i
  *   x            BF16 [M, H]
  *   topk_ids     int32 [M, topk]  (ids outside [0, E) are dropped)
  *   topk_weights float [M, topk]
- *   w1           uint8 [E, 2*Ip, H/2]  E2M1, gate/up interleaved rows
- *   w1_scale     prepacked scales of w1 (moe_prepack_scales_mx with N=2*Ip, K=H)
- *   w2           uint8 [E, H, Ip/2]    E2M1
- *   w2_scale     prepacked scales of w2 (N=H, K=Ip)
+ *   w1           E2M1 codes of w1 [E, 2*Ip, H/2] (gate/up interleaved rows),
+ *                prepacked by moe_prepack_weights_mx (N=2*Ip, K=H)
+ *   w1_scale     scales of w1 prepacked by moe_prepack_scales_mx (N=2*Ip, K=H)
+ *   w2           E2M1 codes of w2 [E, H, Ip/2] prepacked (N=H, K=Ip)
+ *   w2_scale     scales of w2 prepacked (N=H, K=Ip)
  *   out          BF16 [M, H]
  * Ip is the stored (padded) intermediate size; padding rows/columns of the
  * weights must hold zero codes. Tokens without a local route get 0.

@@ -61,7 +61,8 @@ def test_workspace_size_and_layout(L):
         lay = m.fused_moe_workspace_layout(96, 5120, 640, 384, 6, bool(a16))
         assert n == lay["total_bytes"] > 0
         offs = [lay[k] for k in ("status_off", "expert_off_off", "sorted_route_off",
-                                 "sorted_w_off", "block_expert_off", "route_pos_off", "act_off",
+                                 "sorted_w_off", "block_expert_off", "route_pos_off",
+                                 "sort_scratch_off", "act_off",
                                  "inter_off", "acc_off")]
         assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
         assert lay["block_m"] in (16, 32, 64, 128, 256)
@@ -79,13 +80,16 @@ def test_sort_capacity_bound(L):
 
 
 def test_sort_and_quant_reject_bad_arguments(L):
-    args = [FAKE, FAKE, 4, 2, 8, 16, FAKE, FAKE, FAKE, FAKE, FAKE, None, None]
+    args = [FAKE, FAKE, 4, 2, 8, 16, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 0, None]
     bad = list(args); bad[5] = 48
     assert L.moe_sort(*bad) == 2
     bad = list(args); bad[4] = 600
     assert L.moe_sort(*bad) == 2
     bad = list(args); bad[6] = None
     assert L.moe_sort(*bad) == 1
+    big = list(args); big[2] = 5000                    # 10000 routes need histogram scratch
+    assert L.moe_sort_workspace_bytes(5000, 2, 8, 16) == 2 * 8 * 4
+    assert L.moe_sort(*big) == 3                       # no workspace given
     assert L.moe_quant_act_mx(FAKE, 4, 100, 100, FAKE, FAKE, None) == 2   # K % 32
     assert L.moe_quant_act_mx(FAKE, 4, 128, 64, FAKE, FAKE, None) == 1    # ldx < K
     assert L.moe_quant_act_mx(FAKE + 8, 4, 128, 128, FAKE, FAKE, None) == 4

@@ -44,10 +44,11 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_lib, name, Ms):
     for M in Ms:                                   # two calls in a row on the shared scratch
         assert layer.workspace_bytes(M, mi.SHAPES[name].topk) <= m.NOALLOC_WORKSPACE_BYTES
         x, ids, w = _inputs(name, M)
-        want = m.fused_moe_a8w4(x, ids, w, layer.w1, layer.w1_scale, layer.w2, layer.w2_scale)
+        want = m.fused_moe_a8w4(x, ids, w, layer.w1, layer.w1_scale, layer.w2, layer.w2_scale,
+                                layer.E, layer.Ip)
         out = torch.full((M, layer.H), float("nan"), dtype=torch.bfloat16, device="cuda")
         got = m.fused_moe_a8w4_noalloc(x, ids, w, layer.w1, layer.w1_scale, layer.w2,
-                                       layer.w2_scale, out=out)
+                                       layer.w2_scale, layer.E, layer.Ip, out=out)
         torch.cuda.synchronize()
         _check_close(got, want)
 
@@ -60,7 +61,7 @@ def test_noalloc_refuses_shapes_that_do_not_fit(cuda_lib):
     out = torch.zeros(M, layer.H, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(m.MoeError) as exc:
         m.fused_moe_a8w4_noalloc(x, ids, w, layer.w1, layer.w1_scale, layer.w2, layer.w2_scale,
-                                 out=out)
+                                 layer.E, layer.Ip, out=out)
     assert exc.value.code == 3                     # MOE_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert (out.float() == 0).all()                # nothing was launched
