@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = *a.num_padded;
+  pdl_launch_dependents();
   const int total_tiles = a.num_blocks * a.n_tiles;
   const int kblocks = a.K / kTileK;
 
@@ -163,6 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // everything above overlaps the previous kernel; its outputs are read below
+  pdl_wait_prior();
+  const int P = *a.num_padded;
 
   auto stage_ptr = [&](int s) { return smem + s * C::kStageBytes; };
 

@@ -108,26 +108,41 @@ struct Cfg {
   static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
 };
 
-// Position of the producer (or its L2-prefetch look-ahead) in this CTA's
-// sequence of (tile, k-block) pairs.
-struct Cursor {
-  int t, kb, m_blk, n_tile, e;
-  bool valid;
-};
-
 __device__ __forceinline__ void tile_coords(int t, const struct MxArgs& a, int& m_blk, int& n_tile);
 
-// Moves c to the first tile at or after c.t (stride gridDim.x) that holds routes.
-__device__ __forceinline__ void seek_valid(Cursor& c, const MxArgs& a, int total_tiles, int P,
-                                           int bn) {
-  for (; c.t < total_tiles; c.t += gridDim.x) {
-    tile_coords(c.t, a, c.m_blk, c.n_tile);
-    if (c.m_blk * bn >= P) continue;
-    c.e = __ldg(a.block_expert + c.m_blk);
-    if (c.e >= 0 && c.e < a.E) { c.valid = true; return; }
+// This CTA's tiles t = blockIdx.x + i * gridDim.x that hold routes, in order.
+// A tile holds routes iff its route block starts below the padded route count,
+// so the walk needs no memory access; the expert id of the next tile is
+// loaded one tile ahead, off the critical path of every role.
+struct TileSeq {
+  int t, m_blk, n_tile, e;
+  bool valid;
+  int nt, nm, nn, ne;
+  bool nvalid;
+
+  __device__ __forceinline__ static bool find(int& t, int& m, int& n, const MxArgs& a, int total,
+                                              int P, int bn) {
+    for (; t < total; t += gridDim.x) {
+      tile_coords(t, a, m, n);
+      if (m * bn < P) return true;
+    }
+    return false;
   }
-  c.valid = false;
-}
+  __device__ __forceinline__ void init(const MxArgs& a, int total, int P, int bn) {
+    t = blockIdx.x;
+    valid = find(t, m_blk, n_tile, a, total, P, bn);
+    e = valid ? __ldg(a.block_expert + m_blk) : -1;
+    nt = t + gridDim.x;
+    nvalid = valid && find(nt, nm, nn, a, total, P, bn);
+    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+  }
+  __device__ __forceinline__ void next(const MxArgs& a, int total, int P, int bn) {
+    t = nt; m_blk = nm; n_tile = nn; e = ne; valid = nvalid;
+    nt = t + gridDim.x;
+    nvalid = valid && find(nt, nm, nn, a, total, P, bn);
+    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+  }
+};
 
 __device__ __forceinline__ void tile_coords(int t, const MxArgs& a, int& m_blk, int& n_tile) {
   if (a.stage == 1) {  // route-block major: the n-tiles of a block share its activations
@@ -156,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = *a.num_padded;
+  pdl_launch_dependents();
   const int total_tiles = a.num_blocks * a.n_tiles;
   const int kblocks = a.K / kTileK;
 #ifdef MOE_WAIT_STATS
@@ -186,6 +201,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // everything above overlaps the previous kernel; its outputs are read below
+  pdl_wait_prior();
+  const int P = *a.num_padded;
   const uint32_t sf_col0 = C::kAccBufs * C::kAccCols;
 
   if (warp == 0) {
@@ -203,9 +221,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       int stage = 0;
       uint32_t phase = 0;
       uint8_t* sbase = stages;
-      Cursor cur{static_cast<int>(blockIdx.x), 0, 0, 0, 0, false};
-      seek_valid(cur, a, total_tiles, P, BN);
-      Cursor pf = cur;
+      TileSeq cur;
+      cur.init(a, total_tiles, P, BN);
+      TileSeq pf = cur;
+      int pf_kb = 0;
       const uint8_t* pf_w = nullptr;
       auto pf_tile = [&]() {
         pf_w = a.w_base + (static_cast<int64_t>(pf.e) * a.n_tiles + pf.n_tile) * kblocks * kWTile;
@@ -213,11 +232,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       if (pf.valid) pf_tile();
       auto pf_step = [&]() {
         if (!pf.valid) return;
-        bulk_prefetch_l2(pf_w + static_cast<int64_t>(pf.kb) * kWTile, kWTile);
-        if (++pf.kb == kblocks) {
-          pf.kb = 0;
-          pf.t += gridDim.x;
-          seek_valid(pf, a, total_tiles, P, BN);
+        bulk_prefetch_l2(pf_w + static_cast<int64_t>(pf_kb) * kWTile, kWTile);
+        if (++pf_kb == kblocks) {
+          pf_kb = 0;
+          pf.next(a, total_tiles, P, BN);
           if (pf.valid) pf_tile();
         }
       };
@@ -252,8 +270,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             sbase += C::kStageBytes;
           }
         }
-        cur.t += gridDim.x;
-        seek_valid(cur, a, total_tiles, P, BN);
+        cur.next(a, total_tiles, P, BN);
       }
     }
   } else if (warp == 1) {
@@ -273,12 +290,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       uint32_t sdesc_off = 0;                                // stage * kStageStep
       uint32_t sf_tmem = tmem + sf_col0;                      // this stage's scale columns
       int local = 0;
-      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
-        int m_blk, n_tile;
-        tile_coords(t, a, m_blk, n_tile);
-        if (m_blk * BN >= P) continue;
-        const int e = __ldg(a.block_expert + m_blk);
-        if (e < 0 || e >= a.E) continue;
+      TileSeq seq;
+      for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
         ++local;
@@ -331,12 +344,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     const int et = threadIdx.x - 64;         // 0..127
     const int R = a.M * a.topk;
     int local = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      int m_blk, n_tile;
-      tile_coords(t, a, m_blk, n_tile);
-      if (m_blk * BN >= P) continue;
-      const int e = __ldg(a.block_expert + m_blk);
-      if (e < 0 || e >= a.E) continue;
+    TileSeq seq;
+    for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
+      const int m_blk = seq.m_blk, n_tile = seq.n_tile;
       const int ab = local % C::kAccBufs;
       const uint32_t acc_phase = (local / C::kAccBufs) & 1;
       ++local;
@@ -590,6 +600,11 @@ cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t s) {
   cfg.blockDim = dim3(plan.threads);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, plan.kernel, args);
 }
 

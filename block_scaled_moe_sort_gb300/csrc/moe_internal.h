@@ -69,7 +69,5 @@ cudaError_t prepare_gemm_mx(int stage, const GemmArgs& a, GemmPlan* plan);
 cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& a, GemmPlan* plan);
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t s);
 
-cudaError_t launch_stage1_simt(const GemmArgs& a, cudaStream_t s);
-cudaError_t launch_stage2_simt(const GemmArgs& a, cudaStream_t s);
 
 }  // namespace moe

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include "common.cuh"
 #include "moe_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 
@@ -67,6 +68,17 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
   constexpr int kBatch = 5;                 // 32-blocks per lane held at once
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_launch_dependents();
+  // zero the FP32 routing-weighted accumulator (no dependence on the sort)
+  {
+    const int64_t n4 = static_cast<int64_t>(M) * H / 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    float4* a4 = reinterpret_cast<float4*>(acc);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += stride)
+      a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait_prior();   // route positions come from the sort
   if (t < M) {
     // route positions of this token, one per lane
     const int my_pos = lane < topk ? __ldg(route_pos + static_cast<int64_t>(t) * topk + lane) : -1;
@@ -126,12 +138,6 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
       }
     }
   }
-  // zero the FP32 routing-weighted accumulator
-  const int64_t n4 = static_cast<int64_t>(M) * H / 4;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  float4* a4 = reinterpret_cast<float4*>(acc);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
-    a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* __restrict__ scale,
@@ -177,6 +183,7 @@ __global__ void __launch_bounds__(256) prepack_weights_kernel(const uint8_t* __r
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc, int64_t n8,
                                                        __nv_bfloat16* __restrict__ out) {
+  pdl_wait_prior();   // the accumulator comes from stage two
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
@@ -215,12 +222,20 @@ cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, i
   if (topk > 32) return cudaErrorInvalidValue;
   const int grid = (M + 7) / 8 > 0 ? (M + 7) / 8 : 1;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (a16)
-    gather_act_kernel<true><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, route_pos, act, act_sf, acc);
-  else
-    gather_act_kernel<false><<<grid, 256, 0, s>>>(xb, M, H, topk, bm, route_pos, act, act_sf,
-                                                  acc);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, gather_act_kernel<true>, xb, M, H, topk, bm, route_pos, act,
+                              act_sf, acc);
+  return cudaLaunchKernelEx(&cfg, gather_act_kernel<false>, xb, M, H, topk, bm, route_pos, act,
+                            act_sf, acc);
 }
 
 cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uint8_t* out,
@@ -242,9 +257,16 @@ cudaError_t launch_prepack_weights(const uint8_t* w, int E, int N, int K, uint8_
 cudaError_t launch_finalize(const float* acc, int64_t n, void* out, cudaStream_t s) {
   const int64_t n8 = n / 8;
   if (n8 == 0) return cudaSuccess;
-  finalize_kernel<<<grid_for(n8, 256, 152 * 8), 256, 0, s>>>(acc, n8,
-                                                              static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for(n8, 256, 152 * 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, finalize_kernel, acc, n8, static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace moe

@@ -23,6 +23,7 @@
 #include <cstdint>
 #include "common.cuh"
 #include "moe_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_small_kernel(const SortArgs 
   int32_t* off = sm + kWarps * a.E;       // [E + 1]
   int32_t* tot = off + a.E + 1;           // [E]
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  pdl_launch_dependents();   // the next kernel waits for this one to finish anyway
   if (blockIdx.x == 0 && tid == 0 && a.status) a.status[0] = 0;
   const int chunk = warp_chunk(a.R);
   int e[kItems];
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_scatter_kernel(const SortArg
   int32_t* tot = off + a.E + 1;           // [E]
   int32_t* pre = tot + a.E;               // [E] routes of this expert in earlier CTAs
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && tid == 0 && a.status) a.status[0] = 0;
   const int base = blockIdx.x * kRoutesPerCta;
   const int count = min(kRoutesPerCta, a.R - base);
