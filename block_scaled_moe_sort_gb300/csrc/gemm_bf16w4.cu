@@ -26,6 +26,7 @@
 #include "common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
+#include "gemm_tiles.cuh"
 
 namespace moe {
 namespace {
@@ -63,15 +64,21 @@ struct Cfg16 {
   static constexpr int kABytes = 2 * kAAtomBytes;              // 32 KB BF16 weights
   // stage layout: A atoms (1024-aligned), B atoms (1024-aligned), raw, scales
   static constexpr int kStageBytes = (kABytes + kBBytes + kRawBytes + kSfBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN <= 32 ? 4 : (BN <= 64 ? 3 : 2);
+  // Small route blocks run two CTAs per SM: the BF16 MMA has half the K of
+  // the FP8 one, so one issuing thread per SM cannot keep up with HBM.
+  static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
+  static constexpr int kStages = BN <= 32 ? 2 : (BN <= 64 ? 3 : 2);
   static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
   static constexpr int kColsNeeded = kAccBufs * BN;
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64
                                    : kColsNeeded <= 128 ? 128 : kColsNeeded <= 256 ? 256 : 512;
   static constexpr int kEpiFloats = 32 * (64 + 4);
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kEpiFloats * 4 + 256;
+  static constexpr int kRouteBytes = 256 * 8;
+  static constexpr int kSmem =
+      1024 + kStages * kStageBytes + kEpiFloats * 4 + kRouteBytes + 256;
   static constexpr uint32_t kTxBytes = kRawBytes + kSfBytes + kBBytes;
-  static_assert(kSmem <= 227 * 1024, "smem budget");
+  static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
+  static_assert(kColsNeeded <= 512 / kCtasPerSm, "TMEM budget");
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -110,18 +117,10 @@ __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t s) {
   return h | (h << 16);
 }
 
-__device__ __forceinline__ void tile_coords(int t, const Bf16Args& a, int& m_blk, int& n_tile) {
-  if (a.stage == 1) {
-    m_blk = t / a.n_tiles;
-    n_tile = t % a.n_tiles;
-  } else {
-    n_tile = t / a.num_blocks;
-    m_blk = t % a.num_blocks;
-  }
-}
+using Seq16 = TileSeq<Bf16Args>;
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
     moe_gemm_bf16w4_kernel(const __grid_constant__ CUtensorMap tmW,
                            const __grid_constant__ CUtensorMap tmX, const Bf16Args a) {
   using C = Cfg16<BN>;
@@ -129,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   float* epi = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token (stage 2) / -1 pad
+  float* s_w = reinterpret_cast<float*>(s_tok + 256);             // [BN] routing weight
   __shared__ uint64_t full_bar[C::kStages], conv_bar[C::kStages], empty_bar[C::kStages];
   __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint64_t drain_bar;
@@ -171,18 +172,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Weight tiles are contiguous 8 KB blocks fetched by one bulk copy each;
+    // a second cursor runs kPrefetch tiles ahead and prefetches them into L2.
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
+      constexpr int kPrefetch = 8;
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
-        int m_blk, n_tile;
-        tile_coords(t, a, m_blk, n_tile);
-        if (m_blk * BN >= P) continue;
-        const int e = __ldg(a.block_expert + m_blk);
-        if (e < 0 || e >= a.E) continue;
-        const int64_t tile0 = (static_cast<int64_t>(e) * a.n_tiles + n_tile) * kblocks;
+      Seq16 cur;
+      cur.init(a, total_tiles, P, BN);
+      Seq16 pf = cur;
+      int pf_kb = 0;
+      auto pf_step = [&]() {
+        if (!pf.valid) return;
+        const int64_t tile = (static_cast<int64_t>(pf.e) * a.n_tiles + pf.n_tile) * kblocks + pf_kb;
+        bulk_prefetch_l2(a.w + tile * C::kRawBytes, C::kRawBytes);
+        if (++pf_kb == kblocks) {
+          pf_kb = 0;
+          pf.next(a, total_tiles, P, BN);
+        }
+      };
+      for (int i = 0; i < kPrefetch; ++i) pf_step();
+      while (cur.valid && !abort_flag) {
+        const int64_t tile0 = (static_cast<int64_t>(cur.e) * a.n_tiles + cur.n_tile) * kblocks;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
           uint8_t* sb = stage_ptr(stage);
@@ -194,9 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h)
             tma_load_2d(sb + C::kABytes + h * C::kBAtomBytes, &tmX, &full_bar[stage],
-                        kb * kTileK + h * kAtomK, m_blk * BN, pol_x);
+                        kb * kTileK + h * kAtomK, cur.m_blk * BN, pol_x);
+          pf_step();
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
+        cur.next(a, total_tiles, P, BN);
       }
     }
   } else if (warp == 1) {
@@ -208,12 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_dense(1, 1, kTileN, BN);
       const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
       const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kABytes), 16, 1024, kSwizzle128B);
-      for (int t = blockIdx.x; t < total_tiles && !abort_flag; t += gridDim.x) {
-        int m_blk, n_tile;
-        tile_coords(t, a, m_blk, n_tile);
-        if (m_blk * BN >= P) continue;
-        const int e = __ldg(a.block_expert + m_blk);
-        if (e < 0 || e >= a.E) continue;
+      Seq16 seq;
+      for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
         ++local;
@@ -248,12 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = r & 7;
     int stage = 0;
     uint32_t phase = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      int m_blk, n_tile;
-      tile_coords(t, a, m_blk, n_tile);
-      if (m_blk * BN >= P) continue;
-      const int e = __ldg(a.block_expert + m_blk);
-      if (e < 0 || e >= a.E) continue;
+    Seq16 seq;
+    for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
       bool stop = false;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (abort_flag || !mbar_wait(&full_bar[stage], phase, a.status)) {
@@ -293,12 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;
     const int R = a.M * a.topk;
     int local = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      int m_blk, n_tile;
-      tile_coords(t, a, m_blk, n_tile);
-      if (m_blk * BN >= P) continue;
-      const int e = __ldg(a.block_expert + m_blk);
-      if (e < 0 || e >= a.E) continue;
+    Seq16 seq;
+    for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
+      const int m_blk = seq.m_blk, n_tile = seq.n_tile;
       const int ab = local % C::kAccBufs;
       const uint32_t acc_phase = (local / C::kAccBufs) & 1;
       ++local;
@@ -306,6 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
+      named_bar_sync(1, 128);                 // previous tile's readers are done
+      for (int c = et; c < BN; c += 128) {
+        const int rr = __ldg(a.sorted_route + p_base + c);
+        s_tok[c] = rr < R ? rr / a.topk : -1;
+        s_w[c] = __ldg(a.sorted_w + p_base + c);
+      }
+      named_bar_sync(1, 128);
       constexpr int kChunk = BN < 32 ? BN : 32;
       for (int c0 = 0; c0 < BN; c0 += kChunk) {
         float v[32];
@@ -324,21 +335,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r32[i]);
         }
         if (a.stage == 1) {
+          // gate/up pairs in adjacent lanes; even lanes take columns [0, half)
+          constexpr int half = kChunk / 2;
+          const bool odd = lane & 1;
           const int j_local = row >> 1;
           named_bar_sync(1, 128);
 #pragma unroll
-          for (int i = 0; i < kChunk; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
-            if ((lane & 1) == 0) epi[i * 68 + j_local] = silu_mul(v[i], other);
+          for (int k = 0; k < half; ++k) {
+            const float send = odd ? v[k] : v[k + half];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float gate = odd ? recv : v[k];
+            const float up = odd ? v[k + half] : recv;
+            epi[(k + (odd ? half : 0)) * 68 + j_local] = __fdividef(gate, 1.0f + __expf(-gate)) * up;
           }
           named_bar_sync(1, 128);
-          const int item = et >> 1, half = et & 1;
+          const int item = et >> 1, hf = et & 1;
           const int col = item >> 1, blk = item & 1;
           if (col < kChunk) {
             const int64_t p = p_base + c0 + col;
-            const bool pad = __ldg(a.sorted_route + p) >= R;
+            const bool pad = s_tok[c0 + col] < 0;
             const float4* src =
-                reinterpret_cast<const float4*>(epi + col * 68 + blk * 32 + half * 16);
+                reinterpret_cast<const float4*>(epi + col * 68 + blk * 32 + hf * 16);
             uint32_t o[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -348,25 +365,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               o[2 * q] = pad ? 0u : *reinterpret_cast<uint32_t*>(&h0);
               o[2 * q + 1] = pad ? 0u : *reinterpret_cast<uint32_t*>(&h1);
             }
-            const int jcol = n_tile * 64 + blk * 32 + half * 16;
+            const int jcol = n_tile * 64 + blk * 32 + hf * 16;
             uint4* dst = reinterpret_cast<uint4*>(a.inter + p * a.Ip + jcol);
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           }
         } else {
-          int tok = -1;
-          float wgt = 0.f;
-          if (lane < kChunk) {
-            const int64_t p = p_base + c0 + lane;
-            const int rr = __ldg(a.sorted_route + p);
-            if (rr < R) { tok = rr / a.topk; wgt = __ldg(a.sorted_w + p); }
-          }
-          const int n = n_tile * kTileN + row;
+          for (int h = 0; h < kChunk; h += 16) {
+            named_bar_sync(1, 128);
 #pragma unroll
-          for (int i = 0; i < kChunk; ++i) {
-            const int ti = __shfl_sync(0xffffffffu, tok, i);
-            const float wi = __shfl_sync(0xffffffffu, wgt, i);
-            if (ti >= 0) atomicAdd(a.acc + static_cast<int64_t>(ti) * a.H + n, wi * v[i]);
+            for (int i = 0; i < 16; ++i)
+              if (h + i < kChunk) epi[i * 132 + row] = v[h + i];
+            named_bar_sync(1, 128);
+            const int g = et & 31, cb = et >> 5;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = cb + 4 * j;
+              if (h + c >= kChunk) continue;
+              const int tok = s_tok[c0 + h + c];
+              if (tok < 0) continue;
+              const float wgt = s_w[c0 + h + c];
+              float4 f = *reinterpret_cast<const float4*>(epi + c * 132 + 4 * g);
+              f.x *= wgt; f.y *= wgt; f.z *= wgt; f.w *= wgt;
+              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(tok) * a.H +
+                                                  n_tile * kTileN + 4 * g),
+                        f);
+            }
           }
         }
       }
@@ -412,8 +436,9 @@ cudaError_t plan_bn(const Bf16Args& a, int num_sms, GemmPlan* plan) {
   cudaError_t err = ensure_smem_attr(fn, C::kSmem);
   if (err != cudaSuccess) return err;
   const int tiles = a.num_blocks * a.n_tiles;
+  const int slots = num_sms * C::kCtasPerSm;
   plan->kernel = fn;
-  plan->grid = tiles < num_sms ? tiles : num_sms;
+  plan->grid = tiles < slots ? tiles : slots;
   plan->threads = kThreads;
   plan->smem = C::kSmem;
   memcpy(plan->args, &a, sizeof(a));

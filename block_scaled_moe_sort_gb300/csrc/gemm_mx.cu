@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
+#include "gemm_tiles.cuh"
 
 namespace moe {
 namespace {
@@ -87,9 +88,11 @@ struct Cfg {
   // Up to block_m 64 two CTAs share an SM (two MMA-issuing threads: at small
   // N one thread cannot issue tcgen05 work fast enough to keep up with HBM),
   // so ring, accumulators and scale columns are sized for half an SM.
-  static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
-  static constexpr int kStages = BN <= 16 ? 5 : BN <= 32 ? 4 : (BN <= 64 ? 4 : (BN <= 128 ? 6 : 4));
-  static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
+  // block_m 128 also runs two CTAs (single accumulator each: one CTA's
+  // MMAs overlap the other's epilogue).
+  static constexpr int kCtasPerSm = BN <= 128 ? 2 : 1;
+  static constexpr int kStages = BN <= 16 ? 5 : BN <= 32 ? 4 : (BN <= 64 ? 4 : (BN <= 128 ? 3 : 4));
+  static constexpr int kAccBufs = BN <= 64 ? 2 : 1;
   // Independent accumulators per tile: MMA kk of a k-block adds into
   // accumulator kk % kSplit, so small-N MMAs do not form one dependent chain;
   // the epilogue sums them.
@@ -100,7 +103,9 @@ struct Cfg {
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64
                                    : kColsNeeded <= 128 ? 128 : kColsNeeded <= 256 ? 256 : 512;
   static constexpr int kEpiFloats = 32 * (64 + 4);             // stage-1 / stage-2 transpose tile
-  static constexpr int kSmem = 1024 /*align slack*/ + kStages * kStageBytes + kEpiFloats * 4 + 256;
+  static constexpr int kRouteBytes = 256 * 8;                  // per-tile route info
+  static constexpr int kSmem =
+      1024 /*align slack*/ + kStages * kStageBytes + kEpiFloats * 4 + kRouteBytes + 256;
   // TMA transaction bytes of one stage: FP4 A counts packed bytes
   static constexpr uint32_t kTxBytes = kTileN * kTileK / 2 + kBBytes + kSfBytes;
   static_assert(kColsNeeded <= 512 / kCtasPerSm, "TMEM budget");
@@ -108,51 +113,7 @@ struct Cfg {
   static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
 };
 
-__device__ __forceinline__ void tile_coords(int t, const struct MxArgs& a, int& m_blk, int& n_tile);
-
-// This CTA's tiles t = blockIdx.x + i * gridDim.x that hold routes, in order.
-// A tile holds routes iff its route block starts below the padded route count,
-// so the walk needs no memory access; the expert id of the next tile is
-// loaded one tile ahead, off the critical path of every role.
-struct TileSeq {
-  int t, m_blk, n_tile, e;
-  bool valid;
-  int nt, nm, nn, ne;
-  bool nvalid;
-
-  __device__ __forceinline__ static bool find(int& t, int& m, int& n, const MxArgs& a, int total,
-                                              int P, int bn) {
-    for (; t < total; t += gridDim.x) {
-      tile_coords(t, a, m, n);
-      if (m * bn < P) return true;
-    }
-    return false;
-  }
-  __device__ __forceinline__ void init(const MxArgs& a, int total, int P, int bn) {
-    t = blockIdx.x;
-    valid = find(t, m_blk, n_tile, a, total, P, bn);
-    e = valid ? __ldg(a.block_expert + m_blk) : -1;
-    nt = t + gridDim.x;
-    nvalid = valid && find(nt, nm, nn, a, total, P, bn);
-    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
-  }
-  __device__ __forceinline__ void next(const MxArgs& a, int total, int P, int bn) {
-    t = nt; m_blk = nm; n_tile = nn; e = ne; valid = nvalid;
-    nt = t + gridDim.x;
-    nvalid = valid && find(nt, nm, nn, a, total, P, bn);
-    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
-  }
-};
-
-__device__ __forceinline__ void tile_coords(int t, const MxArgs& a, int& m_blk, int& n_tile) {
-  if (a.stage == 1) {  // route-block major: the n-tiles of a block share its activations
-    m_blk = t / a.n_tiles;
-    n_tile = t % a.n_tiles;
-  } else {             // feature-tile major: the FP32 reductions of a tile stay in L2
-    n_tile = t / a.num_blocks;
-    m_blk = t % a.num_blocks;
-  }
-}
+using Seq = TileSeq<MxArgs>;
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
@@ -164,6 +125,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
                                              ~uintptr_t(1023));
   uint8_t* stages = smem;
   float* epi = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token (stage 2) / -1 pad
+  float* s_w = reinterpret_cast<float*>(s_tok + 256);             // [BN] routing weight
   __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
   __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint64_t drain_bar;
@@ -221,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       int stage = 0;
       uint32_t phase = 0;
       uint8_t* sbase = stages;
-      TileSeq cur;
+      Seq cur;
       cur.init(a, total_tiles, P, BN);
-      TileSeq pf = cur;
+      Seq pf = cur;
       int pf_kb = 0;
       const uint8_t* pf_w = nullptr;
       auto pf_tile = [&]() {
@@ -290,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       uint32_t sdesc_off = 0;                                // stage * kStageStep
       uint32_t sf_tmem = tmem + sf_col0;                      // this stage's scale columns
       int local = 0;
-      TileSeq seq;
+      Seq seq;
       for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
@@ -344,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     const int et = threadIdx.x - 64;         // 0..127
     const int R = a.M * a.topk;
     int local = 0;
-    TileSeq seq;
+    Seq seq;
     for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
       const int m_blk = seq.m_blk, n_tile = seq.n_tile;
       const int ab = local % C::kAccBufs;
@@ -361,6 +324,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       tc_fence_after();
       const uint32_t d_tmem = tmem + ab * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
+      // route info of the tile's columns, loaded once: token (or -1 for a pad), weight
+      named_bar_sync(1, 128);                 // previous tile's readers are done
+      for (int c = et; c < BN; c += 128) {
+        const int rr = __ldg(a.sorted_route + p_base + c);
+        s_tok[c] = rr < R ? rr / a.topk : -1;
+        s_w[c] = __ldg(a.sorted_w + p_base + c);
+      }
+      named_bar_sync(1, 128);
       constexpr int kChunk = BN < 32 ? BN : 32;
       for (int c0 = 0; c0 < BN; c0 += kChunk) {
         float v[32];
@@ -381,23 +352,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             v[i] = sp == 0 ? __uint_as_float(r[i]) : v[i] + __uint_as_float(r[i]);
         }
         if (a.stage == 1) {
-          // gate (even row) / up (odd row) pairs sit in adjacent lanes
+          // Gate (row 2j) and up (row 2j+1) sit in adjacent lanes. Even lanes
+          // produce columns [0, half), odd lanes [half, kChunk): one shuffle
+          // per column pair, no divergence.
+          constexpr int half = kChunk / 2;
+          const bool odd = lane & 1;
           const int j_local = row >> 1;       // 0..63
           named_bar_sync(1, 128);             // previous chunk's readers are done
 #pragma unroll
-          for (int i = 0; i < kChunk; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[i], 1);
-            if ((lane & 1) == 0) epi[i * 68 + j_local] = silu_mul(v[i], other);
+          for (int k = 0; k < half; ++k) {
+            const float send = odd ? v[k] : v[k + half];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float gate = odd ? recv : v[k];
+            const float up = odd ? v[k + half] : recv;
+            epi[(k + (odd ? half : 0)) * 68 + j_local] = __fdividef(gate, 1.0f + __expf(-gate)) * up;
           }
           named_bar_sync(1, 128);
           // 2 threads per (route column, 32-block): each quantises 16 values
-          const int item = et >> 1, half = et & 1;     // 64 items
+          const int item = et >> 1, hf = et & 1;       // 64 items
           const int col = item >> 1, blk = item & 1;   // column in chunk, 32-block in tile
           if (col < kChunk) {
             const int64_t p = p_base + c0 + col;
-            const bool pad = __ldg(a.sorted_route + p) >= R;
+            const bool pad = s_tok[c0 + col] < 0;
             float x[16];
-            const float4* src = reinterpret_cast<const float4*>(epi + col * 68 + blk * 32 + half * 16);
+            const float4* src = reinterpret_cast<const float4*>(epi + col * 68 + blk * 32 + hf * 16);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float4 f = src[q];
@@ -423,12 +401,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
                 codes[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
               }
             }
-            const int jcol = n_tile * 64 + blk * 32 + half * 16;   // intermediate column
+            const int jcol = n_tile * 64 + blk * 32 + hf * 16;     // intermediate column
             *reinterpret_cast<uint4*>(a.inter + p * a.Ip + jcol) =
                 make_uint4(codes[0], codes[1], codes[2], codes[3]);
-            if (half == 0) {
+            if (hf == 0) {
               const int ib = jcol / 32;                          // 32-block index along Ip
-              const int rr = static_cast<int>(p % BN);
+              const int rr = c0 + col;                           // row of p inside the block
               const int64_t atom = (static_cast<int64_t>(m_blk) * (a.Ip / 128) + ib / 4) * C::kNa + rr / 128;
               a.inter_sf[atom * 512 + sf_atom_off(rr & 127, ib & 3)] = static_cast<uint8_t>(sb);
             }
@@ -448,13 +426,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             for (int j = 0; j < 4; ++j) {
               const int c = cb + 4 * j;
               if (h + c >= kChunk) continue;
-              const int64_t p = p_base + c0 + h + c;
-              const int rr = __ldg(a.sorted_route + p);
-              if (rr >= R) continue;
-              const float wgt = __ldg(a.sorted_w + p);
+              const int tok = s_tok[c0 + h + c];
+              if (tok < 0) continue;
+              const float wgt = s_w[c0 + h + c];
               float4 f = *reinterpret_cast<const float4*>(epi + c * 132 + 4 * g);
               f.x *= wgt; f.y *= wgt; f.z *= wgt; f.w *= wgt;
-              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(rr / a.topk) * a.H +
+              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(tok) * a.H +
                                                   n_tile * kTileN + 4 * g),
                         f);
             }
