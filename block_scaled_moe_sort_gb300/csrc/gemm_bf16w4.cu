@@ -9,16 +9,23 @@
 //            acc[token(p), n] += w_p * D[n, p]
 //
 // kind::f16 needs both operands in the same 16-bit type, so the MXFP4
-// weights are dequantised in shared memory: every E2M1 value times its E8M0
-// scale is a BF16 number (exact: a 2-bit-mantissa value times a power of two),
-// so the MMA sees exactly the weights the format encodes.
+// weights are dequantised on chip: every E2M1 value times its E8M0 scale is
+// a BF16 number (exact: a 2-bit-mantissa value times a power of two), so the
+// MMA sees exactly the weights the format encodes. The dequantised weight
+// tile never touches shared memory: converter threads write it straight into
+// TMEM (one weight row per TMEM lane) and the MMA reads its A operand from
+// there, so a shared-memory stage holds only the packed FP4 tile, its scales
+// and the activation rows, and the ring can be deep.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
-// issuer, warps 2..5 epilogue (TMEM lane quadrant = warp % 4), warps 6..9
-// converters (one weight row per thread: packed FP4 + scale -> 128-byte
-// swizzled K-major BF16, the layout the MMA descriptor reads).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps
+// 2..5 epilogue (TMEM lane quadrant = warp % 4), warps 6.. converters (4 or
+// 8; quadrant = warp % 4, with 8 warps each converts half of the stage's K).
+// A converter thread decodes its row's FP4 pairs through a 256-entry table of
+// BF16 pairs kept once per lane in shared memory (conflict-free lookups),
+// multiplies by the block scale and stores 32 TMEM columns at a time.
 // Pipeline stage = 128 K-elements: one prepacked 8 KB weight tile, fetched by
-// a single bulk copy, and two 128-byte swizzle atoms of BF16 per operand.
+// TMA with the 64-byte swizzle (conflict-free row reads), its 512-byte scale
+// atom, and two 128-byte swizzle atoms of BF16 activations.
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -31,11 +38,11 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 320;
 constexpr int kTileN = 128;   // weight rows per tile (MMA M)
 constexpr int kTileK = 128;   // K per stage = one prepacked 8 KB weight tile
 constexpr int kMmaK = 16;     // K per tcgen05.mma kind::f16
 constexpr int kAtomK = 64;    // BF16 elements per 128-byte swizzle atom row
+constexpr int kACols = 64;    // TMEM columns of one dequantised 128 x 128 BF16 tile
 
 struct Bf16Args {
   int stage;
@@ -54,31 +61,37 @@ struct Bf16Args {
   int32_t* status;
 };
 
+__host__ __device__ constexpr int pow2_cols(int c) {
+  return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
+}
+
 template <int BN>
 struct Cfg16 {
+  // Small route blocks run two CTAs per SM so that two MMA issuers and two
+  // converter groups share the SM; their TMEM halves hold 3 weight slots each.
+  static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
+  static constexpr int kConvWarps = kCtasPerSm == 2 ? 4 : 8;
+  static constexpr int kThreads = 192 + 32 * kConvWarps;
   static constexpr int kRawBytes = kTileN * kTileK / 2;        // 8 KB packed FP4
   static constexpr int kSfBytes = 512;
   static constexpr int kBAtomBytes = BN * 128;                 // BN rows x 64 BF16
   static constexpr int kBBytes = 2 * kBAtomBytes;
-  static constexpr int kAAtomBytes = kTileN * 128;             // 128 rows x 64 BF16
-  static constexpr int kABytes = 2 * kAAtomBytes;              // 32 KB BF16 weights
-  // stage layout: A atoms (1024-aligned), B atoms (1024-aligned), raw, scales
-  static constexpr int kStageBytes = (kABytes + kBBytes + kRawBytes + kSfBytes + 1023) / 1024 * 1024;
-  // Small route blocks run two CTAs per SM: the BF16 MMA has half the K of
-  // the FP8 one, so one issuing thread per SM cannot keep up with HBM.
-  static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
-  static constexpr int kStages = BN <= 32 ? 2 : (BN <= 64 ? 3 : 2);
+  // stage layout: B atoms, raw FP4 tile (64-byte swizzled), scale atom
+  static constexpr int kStageBytes = (kBBytes + kRawBytes + kSfBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = BN == 16 ? 5 : BN == 32 ? 4 : BN == 64 ? 6 : BN == 128 ? 4 : 2;
+  static constexpr int kASlots = kCtasPerSm == 2 ? 3 : 4;
   static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
-  static constexpr int kColsNeeded = kAccBufs * BN;
-  static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64
-                                   : kColsNeeded <= 128 ? 128 : kColsNeeded <= 256 ? 256 : 512;
+  static constexpr int kAccCol0 = kASlots * kACols;
+  static constexpr int kTmemCols = pow2_cols(kAccCol0 + kAccBufs * BN);
+  static constexpr int kLutWords = 256 * 32;
   static constexpr int kEpiFloats = 32 * (64 + 4);
   static constexpr int kRouteBytes = 256 * 8;
   static constexpr int kSmem =
-      1024 + kStages * kStageBytes + kEpiFloats * 4 + kRouteBytes + 256;
+      1024 + kStages * kStageBytes + kLutWords * 4 + kEpiFloats * 4 + kRouteBytes;
   static constexpr uint32_t kTxBytes = kRawBytes + kSfBytes + kBBytes;
   static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
-  static_assert(kColsNeeded <= 512 / kCtasPerSm, "TMEM budget");
+  static_assert(kAccCol0 + kAccBufs * BN <= kTmemCols && kTmemCols * kCtasPerSm <= 512,
+                "TMEM budget");
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -94,22 +107,13 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&z);
 }
 
-// Four E2M1 codes (code i in bits 4i..4i+3 of p16) -> four BF16 values times
-// the power-of-two scale held twice in scale2. The magnitude of each code is
-// looked up byte-wise (high and low byte of its BF16 pattern, 3-bit index),
-// the sign is bit 3 of the code; the scaling multiply is exact.
-__device__ __forceinline__ void fp4x4_to_bf16(uint32_t p16, uint32_t scale2, uint32_t& w01,
-                                              uint32_t& w23) {
-  const uint32_t sel = p16 & 0x7777u;
-  // |E2M1| = 0, .5, 1, 1.5, 2, 3, 4, 6 -> BF16 0000 3F00 3F80 3FC0 4000 4040 4080 40C0
-  const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel);
-  const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);
-  uint32_t a = prmt(lo, hi, 0x5140u);
-  uint32_t b = prmt(lo, hi, 0x7362u);
-  a |= ((p16 << 12) & 0x8000u) | ((p16 << 24) & 0x80000000u);
-  b |= ((p16 << 4) & 0x8000u) | ((p16 << 16) & 0x80000000u);
-  w01 = bf16x2_mul(a, scale2);
-  w23 = bf16x2_mul(b, scale2);
+// BF16 bit pattern of one E2M1 code: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6
+// (exponent field 126 + e for e = 1..3, the subnormal code 1 is 0.5 = 0x3F00),
+// sign from bit 3.
+__device__ __forceinline__ uint32_t e2m1_bf16_bits(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3, m = c & 1;
+  const uint32_t mag = e == 0 ? (m ? 0x3F00u : 0u) : (((126u + e) << 7) | (m << 6));
+  return mag | ((c & 8u) << 12);
 }
 
 __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t s) {
@@ -120,17 +124,19 @@ __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t s) {
 using Seq16 = TileSeq<Bf16Args>;
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
+__global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     moe_gemm_bf16w4_kernel(const __grid_constant__ CUtensorMap tmW,
                            const __grid_constant__ CUtensorMap tmX, const Bf16Args a) {
   using C = Cfg16<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  float* epi = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
-  int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token (stage 2) / -1 pad
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::kStages * C::kStageBytes);  // [256][32]
+  float* epi = reinterpret_cast<float*>(lut + C::kLutWords);
+  int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token / -1 pad
   float* s_w = reinterpret_cast<float*>(s_tok + 256);             // [BN] routing weight
-  __shared__ uint64_t full_bar[C::kStages], conv_bar[C::kStages], empty_bar[C::kStages];
+  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
+  __shared__ uint64_t a_full[C::kASlots], a_empty[C::kASlots];
   __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
@@ -144,8 +150,11 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&conv_bar[s], 4);
       mbar_init(&empty_bar[s], 1);
+    }
+    for (int j = 0; j < C::kASlots; ++j) {
+      mbar_init(&a_full[j], C::kConvWarps);
+      mbar_init(&a_empty[j], 1);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -154,7 +163,15 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
     fence_mbar_init();
+    prefetch_tmap(&tmW);
     prefetch_tmap(&tmX);
+  }
+  // FP4 pair table: entry b holds the BF16 patterns of codes b & 15 (low
+  // half) and b >> 4 (high half), replicated once per lane so that every
+  // lane reads its own bank.
+  for (int i = threadIdx.x; i < C::kLutWords; i += blockDim.x) {
+    const uint32_t b = static_cast<uint32_t>(i) >> 5;
+    lut[i] = e2m1_bf16_bits(b & 15u) | (e2m1_bf16_bits(b >> 4) << 16);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, C::kTmemCols);
@@ -172,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Weight tiles are contiguous 8 KB blocks fetched by one bulk copy each;
-    // a second cursor runs kPrefetch tiles ahead and prefetches them into L2.
+    // A second cursor runs kPrefetch weight tiles ahead and prefetches them
+    // (contiguous 8 KB blocks) into L2.
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
@@ -200,13 +217,13 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
           uint8_t* sb = stage_ptr(stage);
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-          bulk_load(sb + C::kABytes + C::kBBytes, a.w + (tile0 + kb) * C::kRawBytes,
-                    C::kRawBytes, &full_bar[stage], pol_w);
-          bulk_load(sb + C::kABytes + C::kBBytes + C::kRawBytes, a.sfa + (tile0 + kb) * 512, 512,
+          tma_load_2d(sb + C::kBBytes, &tmW, &full_bar[stage], 0,
+                      static_cast<int32_t>((tile0 + kb) * kTileN), pol_w);
+          bulk_load(sb + C::kBBytes + C::kRawBytes, a.sfa + (tile0 + kb) * 512, 512,
                     &full_bar[stage], pol_w);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            tma_load_2d(sb + C::kABytes + h * C::kBAtomBytes, &tmX, &full_bar[stage],
+            tma_load_2d(sb + h * C::kBAtomBytes, &tmX, &full_bar[stage],
                         kb * kTileK + h * kAtomK, cur.m_blk * BN, pol_x);
           pf_step();
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -217,12 +234,11 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, aphase = 0;
       int local = 0;
       constexpr uint32_t idesc = idesc_dense(1, 1, kTileN, BN);
-      const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
-      const uint64_t b_desc0 = smem_desc(smem_u32(smem + C::kABytes), 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
       Seq16 seq;
       for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
@@ -230,22 +246,25 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
         ++local;
         if (!mbar_wait(&acc_empty[ab], acc_phase ^ 1, a.status)) { abort_flag = 1; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + ab * BN;
+        const uint32_t d_tmem = tmem + C::kAccCol0 + ab * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, a.status) ||
-              !mbar_wait(&conv_bar[stage], phase, a.status)) { abort_flag = 1; break; }
+              !mbar_wait(&a_full[slot], aphase, a.status)) { abort_flag = 1; break; }
           tc_fence_after();
-          const uint64_t ad = a_desc0 + static_cast<uint64_t>(stage) * (C::kStageBytes >> 4);
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (C::kStageBytes >> 4);
+          const uint32_t a_tmem = tmem + slot * kACols;
 #pragma unroll
           for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
-            // descriptor units (16 B): atom h of the operand, then 32 B per MMA
+            // B: atom h of the stage, then 32 bytes (2 descriptor units) per MMA;
+            // A: 8 TMEM columns (16 BF16) per MMA
             const int h = kk / (kAtomK / kMmaK), off = (kk % (kAtomK / kMmaK)) * 2;
-            mma_f16(d_tmem, ad + h * (C::kAAtomBytes >> 4) + off, bd + h * (C::kBAtomBytes >> 4) + off,
-                    idesc, (kb | kk) != 0);
+            mma_f16_tmem_a(d_tmem, a_tmem + kk * (kMmaK / 2),
+                           bd + h * (C::kBAtomBytes >> 4) + off, idesc, (kb | kk) != 0);
           }
           tc_commit(&empty_bar[stage]);
+          tc_commit(&a_empty[slot]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+          if (++slot == C::kASlots) { slot = 0; aphase ^= 1; }
         }
         tc_commit(&acc_full[ab]);
       }
@@ -254,42 +273,54 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
     }
   } else if (warp >= 6) {
     // ---------------------------------------------------------- converters
-    const int r = threadIdx.x - 192;                     // weight row 0..127
+    constexpr int kHalves = C::kConvWarps == 8 ? 1 : 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;                      // weight row = TMEM lane
+    const int h0 = C::kConvWarps == 8 ? (warp - 6) >> 2 : 0;
+    const int swz = (r >> 1) & 3;                        // 64-byte swizzle of row r
     const int sf_off = sf_atom_off(r, 0);                // its 4 scale bytes
-    const int sw = r & 7;
-    int stage = 0;
-    uint32_t phase = 0;
+    const uint32_t* lut_lane = lut + lane;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, aphase = 0;
     Seq16 seq;
     for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
       bool stop = false;
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (abort_flag || !mbar_wait(&full_bar[stage], phase, a.status)) {
+        if (abort_flag || !mbar_wait(&full_bar[stage], phase, a.status) ||
+            !mbar_wait(&a_empty[slot], aphase ^ 1, a.status)) {
           abort_flag = 1; stop = true; break;
         }
-        uint8_t* sb = stage_ptr(stage);
-        const uint4* raw = reinterpret_cast<const uint4*>(sb + C::kABytes + C::kBBytes + r * 64);
-        const uint32_t sfw = *reinterpret_cast<const uint32_t*>(sb + C::kABytes + C::kBBytes +
-                                                               C::kRawBytes + sf_off);
+        tc_fence_after();
+        const uint8_t* raw = stage_ptr(stage) + C::kBBytes + r * 64;
+        const uint32_t sfw =
+            *reinterpret_cast<const uint32_t*>(stage_ptr(stage) + C::kBBytes + C::kRawBytes + sf_off);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {                    // 32 elements = one scale block
-          const uint4 v = raw[q];
-          const uint32_t sc = e8m0_bf16x2((sfw >> (8 * q)) & 0xFF);
-          const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-          const int h = q >> 1;                          // swizzle atom (64 elements)
-          uint8_t* dst_row = sb + h * C::kAAtomBytes + r * 128;
+        for (int hh = 0; hh < kHalves; ++hh) {
+          const int h = h0 + hh;                         // 64-element half of the stage
+          uint32_t out[32];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {                  // 8 elements -> one 16-byte chunk
-            uint32_t o0, o1, o2, o3;
-            fp4x4_to_bf16(words[j] & 0xFFFFu, sc, o0, o1);
-            fp4x4_to_bf16(words[j] >> 16, sc, o2, o3);
-            const int c = (q & 1) * 4 + j;               // chunk index 0..7 in the atom row
-            *reinterpret_cast<uint4*>(dst_row + ((c ^ sw) << 4)) = make_uint4(o0, o1, o2, o3);
+          for (int cc = 0; cc < 2; ++cc) {               // 32 elements = one scale block
+            const int c = 2 * h + cc;
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ swz) << 4));
+            const uint32_t sc = e8m0_bf16x2((sfw >> (8 * c)) & 0xFF);
+            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const uint32_t idx = prmt(words[wi], 0u, 0x4440u | b);
+                out[cc * 16 + wi * 4 + b] = bf16x2_mul(lut_lane[idx * 32], sc);
+              }
           }
+          tmem_st_32x32b_x32(t_row + slot * kACols + h * 32, out);
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&conv_bar[stage]);
+        if (lane == 0) mbar_arrive(&a_full[slot]);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        if (++slot == C::kASlots) { slot = 0; aphase ^= 1; }
       }
       if (stop) break;
     }
@@ -308,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, Cfg16<BN>::kCtasPerSm)
       ++local;
       if (abort_flag || !mbar_wait(&acc_full[ab], acc_phase, a.status)) { abort_flag = 1; break; }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t d_tmem =
+          tmem + C::kAccCol0 + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
       named_bar_sync(1, 128);                 // previous tile's readers are done
       for (int c = et; c < BN; c += 128) {
@@ -439,7 +471,7 @@ cudaError_t plan_bn(const Bf16Args& a, int num_sms, GemmPlan* plan) {
   const int slots = num_sms * C::kCtasPerSm;
   plan->kernel = fn;
   plan->grid = tiles < slots ? tiles : slots;
-  plan->threads = kThreads;
+  plan->threads = C::kThreads;
   plan->smem = C::kSmem;
   memcpy(plan->args, &a, sizeof(a));
   return cudaSuccess;
@@ -467,7 +499,11 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   const void* xb = stage == 1 ? g.act : g.inter;
   CUtensorMap* tw = reinterpret_cast<CUtensorMap*>(plan->tmap_a);
   CUtensorMap* tx = reinterpret_cast<CUtensorMap*>(plan->tmap_b);
-  memset(tw, 0, sizeof(CUtensorMap));   // weights arrive by bulk copy; no tensor map needed
+  // packed weight tiles as rows of 64 bytes, one 128-row box per tile, 64-byte swizzle
+  const uint64_t w_rows = static_cast<uint64_t>(g.E) * a.n_tiles * (a.K / kTileK) * kTileN;
+  if (!encode_2d(tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, 64, w_rows, 64, 64, kTileN,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   if (!encode_2d(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a.K, static_cast<uint64_t>(g.p_max),
                  static_cast<uint64_t>(a.K) * 2, kAtomK, g.bm, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
