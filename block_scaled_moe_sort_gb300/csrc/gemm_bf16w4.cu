@@ -129,8 +129,9 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
                            const __grid_constant__ CUtensorMap tmX, const Bf16Args a) {
   using C = Cfg16<BN>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base, derived by pointer arithmetic so that the
+  // compiler keeps every access below in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::kStages * C::kStageBytes);  // [256][32]
   float* epi = reinterpret_cast<float*>(lut + C::kLutWords);
   int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token / -1 pad

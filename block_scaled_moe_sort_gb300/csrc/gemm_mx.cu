@@ -121,8 +121,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
                        const __grid_constant__ CUtensorMap tmB, const MxArgs a) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base, derived by pointer arithmetic so that the
+  // compiler keeps every access below in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = smem;
   float* epi = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token (stage 2) / -1 pad
