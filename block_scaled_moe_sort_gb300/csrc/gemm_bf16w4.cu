@@ -34,6 +34,9 @@
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
 #include "gemm_tiles.cuh"
+#include "timeline.cuh"
+
+MOE_TL_DEFINE(moe_tl_dump_bf16)
 
 namespace moe {
 namespace {
@@ -145,6 +148,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
+  if (threadIdx.x == 0) MOE_TL(3 + a.stage, 0);
   const int total_tiles = a.num_blocks * a.n_tiles;
   const int kblocks = a.K / kTileK;
 
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   const uint32_t tmem = tmem_slot;
   // everything above overlaps the previous kernel; its outputs are read below
   pdl_wait_prior();
+  if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
   const int P = *a.num_padded;
 
   auto stage_ptr = [&](int s) { return smem + s * C::kStageBytes; };
@@ -200,6 +205,9 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       uint32_t phase = 0;
       Seq16 cur;
       cur.init(a, total_tiles, P, BN);
+#ifdef MOE_TIMELINE
+      int tl_first = 1;
+#endif
       Seq16 pf = cur;
       int pf_kb = 0;
       auto pf_step = [&]() {
@@ -218,6 +226,9 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
           uint8_t* sb = stage_ptr(stage);
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+#ifdef MOE_TIMELINE
+          if (tl_first) { MOE_TL(3 + a.stage, 2); tl_first = 0; }
+#endif
           tma_load_2d(sb + C::kBBytes, &tmW, &full_bar[stage], 0,
                       static_cast<int32_t>((tile0 + kb) * kTileN), pol_w);
           bulk_load(sb + C::kBBytes + C::kRawBytes, a.sfa + (tile0 + kb) * 512, 512,
@@ -238,6 +249,9 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       int stage = 0, slot = 0;
       uint32_t phase = 0, aphase = 0;
       int local = 0;
+#ifdef MOE_TIMELINE
+      int tl_mma = 1;
+#endif
       constexpr uint32_t idesc = idesc_dense(1, 1, kTileN, BN);
       const uint64_t b_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
       Seq16 seq;
@@ -251,6 +265,9 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, a.status) ||
               !mbar_wait(&a_full[slot], aphase, a.status)) { abort_flag = 1; break; }
+#ifdef MOE_TIMELINE
+          if (tl_mma) { MOE_TL(3 + a.stage, 3); tl_mma = 0; }
+#endif
           tc_fence_after();
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (C::kStageBytes >> 4);
           const uint32_t a_tmem = tmem + slot * kACols;
@@ -269,6 +286,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         }
         tc_commit(&acc_full[ab]);
       }
+      MOE_TL(3 + a.stage, 4);
       tc_commit(&drain_bar);
       mbar_wait(&drain_bar, 0, a.status);
     }
@@ -431,12 +449,16 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
+    if (threadIdx.x == 64) MOE_TL(3 + a.stage, 5);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    MOE_TL(3 + a.stage, 7);
   }
 }
 

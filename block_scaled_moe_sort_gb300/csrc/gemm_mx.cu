@@ -37,6 +37,9 @@
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
 #include "gemm_tiles.cuh"
+#include "timeline.cuh"
+
+MOE_TL_DEFINE(moe_tl_dump_mx)
 
 namespace moe {
 namespace {
@@ -136,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
+  if (threadIdx.x == 0) MOE_TL(3 + a.stage, 0);
   const int total_tiles = a.num_blocks * a.n_tiles;
   const int kblocks = a.K / kTileK;
 #ifdef MOE_WAIT_STATS
@@ -167,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
   const uint32_t tmem = tmem_slot;
   // everything above overlaps the previous kernel; its outputs are read below
   pdl_wait_prior();
+  if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
   const int P = *a.num_padded;
   const uint32_t sf_col0 = C::kAccBufs * C::kAccCols;
 
@@ -187,6 +192,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       uint8_t* sbase = stages;
       Seq cur;
       cur.init(a, total_tiles, P, BN);
+#ifdef MOE_TIMELINE
+      int tl_first = 1;
+#endif
       Seq pf = cur;
       int pf_kb = 0;
       const uint8_t* pf_w = nullptr;
@@ -217,6 +225,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             WAIT_ADD(0);
           }
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+#ifdef MOE_TIMELINE
+          if (tl_first) { MOE_TL(3 + a.stage, 2); tl_first = 0; }
+#endif
           tma_load_2d(sbase, &tmA, &full_bar[stage], 0, row_a, pol_w);
           tma_load_2d(sbase + C::kABytes, &tmB, &full_bar[stage], kb * kTileK, row_b, pol_x);
           bulk_load(sbase + C::kABytes + C::kBBytes, sfa, 512, &full_bar[stage], pol_w);
@@ -255,6 +266,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       uint32_t sf_tmem = tmem + sf_col0;                      // this stage's scale columns
       int local = 0;
       Seq seq;
+#ifdef MOE_TIMELINE
+      int tl_mma = 1;
+#endif
       for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
@@ -272,6 +286,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             if (!mbar_wait(&full_bar[stage], phase, a.status)) { abort_flag = 1; break; }
             WAIT_ADD(1);
           }
+#ifdef MOE_TIMELINE
+          if (tl_mma) { MOE_TL(3 + a.stage, 3); tl_mma = 0; }
+#endif
           tmem_cp_32x128b_warpx4(sf_tmem, sf_desc0 + sdesc_off);
 #pragma unroll
           for (int j = 0; j < C::kNa; ++j)
@@ -298,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
         tc_commit(&acc_full[ab]);
       }
       // every MMA issued by this thread has finished before TMEM is released
+      MOE_TL(3 + a.stage, 4);
       tc_commit(&drain_bar);
       mbar_wait(&drain_bar, 0, a.status);
     }
@@ -448,12 +466,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
                   static_cast<unsigned long long>(clock64() - _busy0));
 #endif
     }
+    if (threadIdx.x == 64) MOE_TL(3 + a.stage, 5);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    MOE_TL(3 + a.stage, 7);
   }
 #ifdef MOE_WAIT_STATS
   if (threadIdx.x == 0)

@@ -11,6 +11,9 @@
 #include "common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
+#include "timeline.cuh"
+
+MOE_TL_DEFINE(moe_tl_dump_quant)
 
 namespace moe {
 
@@ -69,6 +72,7 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_launch_dependents();
+  if (threadIdx.x == 0) MOE_TL(3, 0);
   // zero the FP32 routing-weighted accumulator (no dependence on the sort)
   {
     const int64_t n4 = static_cast<int64_t>(M) * H / 4;
@@ -79,6 +83,7 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
       a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   pdl_wait_prior();   // route positions come from the sort
+  if (threadIdx.x == 0) MOE_TL(3, 1);
   if (t < M) {
     // route positions of this token, one per lane
     const int my_pos = lane < topk ? __ldg(route_pos + static_cast<int64_t>(t) * topk + lane) : -1;
@@ -138,6 +143,7 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
       }
     }
   }
+  if (threadIdx.x == 0) MOE_TL(3, 7);
 }
 
 __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* __restrict__ scale,
@@ -183,7 +189,9 @@ __global__ void __launch_bounds__(256) prepack_weights_kernel(const uint8_t* __r
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__ acc, int64_t n8,
                                                        __nv_bfloat16* __restrict__ out) {
+  if (threadIdx.x == 0) MOE_TL(6, 0);
   pdl_wait_prior();   // the accumulator comes from stage two
+  if (threadIdx.x == 0) MOE_TL(6, 1);
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
@@ -197,6 +205,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float* __restrict__
     u.w = *reinterpret_cast<uint32_t*>(&h3);
     reinterpret_cast<uint4*>(out)[i] = u;
   }
+  if (threadIdx.x == 0) MOE_TL(6, 7);
 }
 
 int grid_for(int64_t work, int per_cta, int cap) {

@@ -24,6 +24,9 @@
 #include "common.cuh"
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
+#include "timeline.cuh"
+
+MOE_TL_DEFINE(moe_tl_dump_sort)
 
 namespace moe {
 namespace {
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_small_kernel(const SortArgs 
   int32_t* tot = off + a.E + 1;           // [E]
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   pdl_launch_dependents();   // the next kernel waits for this one to finish anyway
+  if (tid == 0) MOE_TL(0, 0);
   if (blockIdx.x == 0 && tid == 0 && a.status) a.status[0] = 0;
   const int chunk = warp_chunk(a.R);
   int e[kItems];
@@ -212,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_small_kernel(const SortArgs 
   __syncthreads();
   scatter(a, e, wt, 0, a.R, chunk, w, lane, cnt + w * a.E, off, blockIdx.x, gridDim.x);
   finish_layout(a, off, tot, blockIdx.x, gridDim.x);
+  if (tid == 0) MOE_TL(0, 7);
 }
 
 // Multi-CTA, pass 1: CTA c writes the expert histogram of its slice to hist[c].
@@ -219,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_count_kernel(const SortArgs 
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;                      // [kWarps][E]
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) MOE_TL(1, 0);
   const int base = blockIdx.x * kRoutesPerCta;
   const int count = min(kRoutesPerCta, a.R - base);
   const int chunk = warp_chunk(count);
@@ -235,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_count_kernel(const SortArgs 
     for (int ww = 0; ww < kWarps; ++ww) s += cnt[ww * a.E + x];
     a.hist[static_cast<int64_t>(blockIdx.x) * a.E + x] = s;
   }
+  if (tid == 0) MOE_TL(1, 7);
 }
 
 // Multi-CTA, pass 2: combine the histograms, then scatter; CTA 0 also writes
@@ -247,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_scatter_kernel(const SortArg
   int32_t* pre = tot + a.E;               // [E] routes of this expert in earlier CTAs
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   pdl_launch_dependents();
+  if (tid == 0) MOE_TL(2, 0);
   if (blockIdx.x == 0 && tid == 0 && a.status) a.status[0] = 0;
   const int base = blockIdx.x * kRoutesPerCta;
   const int count = min(kRoutesPerCta, a.R - base);
@@ -281,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) sort_scatter_kernel(const SortArg
   __syncthreads();
   scatter(a, e, wt, base, count, chunk, w, lane, cnt + w * a.E, off, 0, 1);
   finish_layout(a, off, tot, blockIdx.x, gridDim.x);
+  if (tid == 0) MOE_TL(2, 7);
 }
 
 size_t smem_bytes(int E) { return sizeof(int32_t) * (static_cast<size_t>(kWarps) * E + 3 * E + 1); }
