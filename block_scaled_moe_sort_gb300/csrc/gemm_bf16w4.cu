@@ -356,18 +356,24 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       const int ab = local % C::kAccBufs;
       const uint32_t acc_phase = (local / C::kAccBufs) & 1;
       ++local;
+      // Route info of the tile's columns (token or -1 for a pad, weight),
+      // loaded before waiting for the accumulator.
+      {
+        const int64_t pb = static_cast<int64_t>(m_blk) * BN;
+        named_bar_sync(1, 128);               // previous tile's readers are done
+        for (int c = et; c < BN; c += 128) {
+          const int rr = __ldg(a.sorted_route + pb + c);
+          const int tok = rr < R ? rr / a.topk : -1;
+          s_tok[c] = tok;
+          s_w[c] = __ldg(a.sorted_w + pb + c);
+        }
+        named_bar_sync(1, 128);
+      }
       if (abort_flag || !mbar_wait(&acc_full[ab], acc_phase, a.status)) { abort_flag = 1; break; }
       tc_fence_after();
       const uint32_t d_tmem =
           tmem + C::kAccCol0 + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
-      named_bar_sync(1, 128);                 // previous tile's readers are done
-      for (int c = et; c < BN; c += 128) {
-        const int rr = __ldg(a.sorted_route + p_base + c);
-        s_tok[c] = rr < R ? rr / a.topk : -1;
-        s_w[c] = __ldg(a.sorted_w + p_base + c);
-      }
-      named_bar_sync(1, 128);
       constexpr int kChunk = BN < 32 ? BN : 32;
       for (int c0 = 0; c0 < BN; c0 += kChunk) {
         float v[32];
@@ -422,26 +428,15 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           }
         } else {
-          for (int h = 0; h < kChunk; h += 16) {
-            named_bar_sync(1, 128);
+          // stage 2: this thread holds output feature `row` of the tile for
+          // the chunk's routes, so a warp adds 32 consecutive features (128
+          // contiguous bytes of one token row) per reduction, from registers
+          const int64_t col = static_cast<int64_t>(n_tile) * kTileN + row;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (h + i < kChunk) epi[i * 132 + row] = v[h + i];
-            named_bar_sync(1, 128);
-            const int g = et & 31, cb = et >> 5;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c = cb + 4 * j;
-              if (h + c >= kChunk) continue;
-              const int tok = s_tok[c0 + h + c];
-              if (tok < 0) continue;
-              const float wgt = s_w[c0 + h + c];
-              float4 f = *reinterpret_cast<const float4*>(epi + c * 132 + 4 * g);
-              f.x *= wgt; f.y *= wgt; f.z *= wgt; f.w *= wgt;
-              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(tok) * a.H +
-                                                  n_tile * kTileN + 4 * g),
-                        f);
-            }
+          for (int i = 0; i < kChunk; ++i) {
+            const int tok = s_tok[c0 + i];
+            if (tok < 0) continue;
+            atomicAdd(a.acc + static_cast<int64_t>(tok) * a.H + col, v[i] * s_w[c0 + i]);
           }
         }
       }

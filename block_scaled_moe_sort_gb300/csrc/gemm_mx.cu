@@ -332,6 +332,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       const int ab = local % C::kAccBufs;
       const uint32_t acc_phase = (local / C::kAccBufs) & 1;
       ++local;
+      // Route info of the tile's columns (token or -1 for a pad, weight),
+      // loaded before waiting for the accumulator.
+      {
+        const int64_t pb = static_cast<int64_t>(m_blk) * BN;
+        named_bar_sync(1, 128);               // previous tile's readers are done
+        for (int c = et; c < BN; c += 128) {
+          const int rr = __ldg(a.sorted_route + pb + c);
+          const int tok = rr < R ? rr / a.topk : -1;
+          s_tok[c] = tok;
+          s_w[c] = __ldg(a.sorted_w + pb + c);
+        }
+        named_bar_sync(1, 128);
+      }
       {
         WAIT_T0();
         if (abort_flag || !mbar_wait(&acc_full[ab], acc_phase, a.status)) { abort_flag = 1; break; }
@@ -343,14 +356,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       tc_fence_after();
       const uint32_t d_tmem = tmem + ab * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
-      // route info of the tile's columns, loaded once: token (or -1 for a pad), weight
-      named_bar_sync(1, 128);                 // previous tile's readers are done
-      for (int c = et; c < BN; c += 128) {
-        const int rr = __ldg(a.sorted_route + p_base + c);
-        s_tok[c] = rr < R ? rr / a.topk : -1;
-        s_w[c] = __ldg(a.sorted_w + p_base + c);
-      }
-      named_bar_sync(1, 128);
       constexpr int kChunk = BN < 32 ? BN : 32;
       for (int c0 = 0; c0 < BN; c0 += kChunk) {
         float v[32];
@@ -431,29 +436,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             }
           }
         } else {
-          // stage 2: transpose the chunk through shared memory so that each
-          // thread owns 4 consecutive features of one route and adds them
-          // with one 16-byte reduction (a warp covers 512 contiguous bytes)
-          for (int h = 0; h < kChunk; h += 16) {
-            named_bar_sync(1, 128);
+          // stage 2: this thread holds output feature `row` of the tile for
+          // the chunk's routes, so a warp adds 32 consecutive features (128
+          // contiguous bytes of one token row) per reduction, from registers
+          const int64_t col = static_cast<int64_t>(n_tile) * kTileN + row;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (h + i < kChunk) epi[i * 132 + row] = v[h + i];
-            named_bar_sync(1, 128);
-            const int g = et & 31, cb = et >> 5;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c = cb + 4 * j;
-              if (h + c >= kChunk) continue;
-              const int tok = s_tok[c0 + h + c];
-              if (tok < 0) continue;
-              const float wgt = s_w[c0 + h + c];
-              float4 f = *reinterpret_cast<const float4*>(epi + c * 132 + 4 * g);
-              f.x *= wgt; f.y *= wgt; f.z *= wgt; f.w *= wgt;
-              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(tok) * a.H +
-                                                  n_tile * kTileN + 4 * g),
-                        f);
-            }
+          for (int i = 0; i < kChunk; ++i) {
+            const int tok = s_tok[c0 + i];
+            if (tok < 0) continue;
+            atomicAdd(a.acc + static_cast<int64_t>(tok) * a.H + col, v[i] * s_w[c0 + i]);
           }
         }
       }

@@ -82,11 +82,13 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
          i += stride)
       a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  if (threadIdx.x == 0) MOE_TL(3, 2);
   pdl_wait_prior();   // route positions come from the sort
   if (threadIdx.x == 0) MOE_TL(3, 1);
   if (t < M) {
     // route positions of this token, one per lane
     const int my_pos = lane < topk ? __ldg(route_pos + static_cast<int64_t>(t) * topk + lane) : -1;
+    if (threadIdx.x == 0) MOE_TL_AFTER(3, 3, my_pos);
     const __nv_bfloat16* xr = x + static_cast<int64_t>(t) * H;
     const int nblk = H / 32;
     const int atoms = (bm + 127) / 128;
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
             }
             sb = quant_block32(v, c);
           }
+          if (threadIdx.x == 0 && i == 0) MOE_TL_AFTER(3, 4, sb);
           for (int j = 0; j < topk; ++j) {
             const int p = __shfl_sync(0xffffffffu, my_pos, j);
             if (p < 0 || !in) continue;
@@ -143,6 +146,10 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
       }
     }
   }
+  if (threadIdx.x == 0) MOE_TL(3, 5);
+#ifdef MOE_TIMELINE
+  __syncthreads();
+#endif
   if (threadIdx.x == 0) MOE_TL(3, 7);
 }
 

@@ -7,7 +7,9 @@
 // Kernel ids: 0 sort (single launch), 1 sort count, 2 sort scatter,
 // 3 gather/quant, 4 stage-1 GEMM, 5 stage-2 GEMM, 6 finalize.
 // Points:     0 entry, 1 wait returned, 2 first load issued, 3 first k-block
-//             ready, 4 last MMA committed, 5 last epilogue done, 7 exit.
+//             ready, 4 last MMA committed, 5 last epilogue done, 7 exit
+//             (gather: 2 zeroing done, 3 route positions in, 4 first block
+//             quantised, 5 stores issued).
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -22,6 +24,12 @@
       cudaMemcpyToSymbol(g_moe_tl, zeros, sizeof(zeros));                               \
     }                                                                                   \
   }
+// Stamp after `value` has been computed (orders the timer read behind it).
+#define MOE_TL_AFTER(kernel, point, value)                                               \
+  do {                                                                                  \
+    asm volatile("" ::"r"(static_cast<uint32_t>(value)));                               \
+    MOE_TL(kernel, point);                                                              \
+  } while (0)
 #define MOE_TL(kernel, point)                                                            \
   do {                                                                                  \
     unsigned long long t_;                                                              \
@@ -31,4 +39,5 @@
 #else
 #define MOE_TL_DEFINE(dump_name)
 #define MOE_TL(kernel, point) ((void)0)
+#define MOE_TL_AFTER(kernel, point, value) ((void)0)
 #endif
