@@ -43,6 +43,30 @@ SWEEP = mi.TOKENS["backbone"]
 L2_FLUSH_BYTES = 256 << 20
 
 
+def recorded_traffic(kernel: str, M: int):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture of the
+    bench workload, or None when the capture is for another kernel or
+    workload, or the kernel sources changed since it was taken (the record
+    holds a SHA-256 of them)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel") != kernel or M != 768:
+        return None
+    h = hashlib.sha256()
+    for f in rec.get("source_files", []):
+        try:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        except OSError:
+            return None
+    if h.hexdigest() != rec.get("source_sha256"):
+        return None
+    return int(rec["traffic_bytes_per_launch"])
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -323,7 +347,8 @@ def main():
     dom_ms = kmean[dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-            "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+            "unit": "GB/s", "frac": round(achieved / hbm, 4),
+            "traffic": recorded_traffic(dom, M),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
             "algorithmic_bytes": int(dom_bytes), "kernel_us": round(dom_ms * 1000, 2)}
 
