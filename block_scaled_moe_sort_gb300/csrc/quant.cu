@@ -58,19 +58,27 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
   }
 }
 
-// One warp per token: the token row is read once (all of a lane's 16-byte
-// loads issued before any use), quantised once (a8w4), and written to the
-// sorted position of each of its routes, scale bytes into the route block's
-// MMA atoms. Rows of pad entries are never written: their GEMM columns are
+// One warp per (token, 32 consecutive 32-element blocks of its row): a lane's
+// block is read once (four 16-byte loads, issued before the wait on the
+// sort), quantised once (a8w4) and written to the sorted position of each of
+// the token's routes: 32 code bytes per lane, a full sector, and the four
+// scale bytes of a 128-column slab combined across four lanes into one
+// aligned 4-byte word of the route block's MMA scale atom (single bytes
+// scattered over the atoms were partial-sector writes that stalled the
+// stores). Rows of pad entries are never written: their GEMM columns are
 // discarded by both epilogues. The CTAs also zero the FP32 accumulator.
 template <bool A16>
 __global__ void __launch_bounds__(256) gather_act_kernel(
     const __nv_bfloat16* __restrict__ x, int M, int H, int topk, int bm,
     const int32_t* __restrict__ route_pos, void* __restrict__ act, uint8_t* __restrict__ act_sf,
     float* __restrict__ acc) {
-  constexpr int kBatch = 5;                 // 32-blocks per lane held at once
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int nblk = H / 32;
+  const int chunks = (nblk + 31) / 32;
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int t = wid / chunks;
+  const int b = (wid % chunks) * 32 + lane;
+  const bool in = t < M && b < nblk;
   pdl_launch_dependents();
   if (threadIdx.x == 0) MOE_TL(3, 0);
   // zero the FP32 routing-weighted accumulator (no dependence on the sort)
@@ -82,75 +90,66 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
          i += stride)
       a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  uint4 raw[4];
+  if (in) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H + b * 32);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) raw[q] = __ldg(src + q);
+  }
   if (threadIdx.x == 0) MOE_TL(3, 2);
   pdl_wait_prior();   // route positions come from the sort
   if (threadIdx.x == 0) MOE_TL(3, 1);
-  if (t < M) {
-    // route positions of this token, one per lane
-    const int my_pos = lane < topk ? __ldg(route_pos + static_cast<int64_t>(t) * topk + lane) : -1;
-    if (threadIdx.x == 0) MOE_TL_AFTER(3, 3, my_pos);
-    const __nv_bfloat16* xr = x + static_cast<int64_t>(t) * H;
-    const int nblk = H / 32;
-    const int atoms = (bm + 127) / 128;
-    const int nslab = H / 128;
-    for (int b0 = 0; b0 < nblk; b0 += 32 * kBatch) {
-      uint4 raw[kBatch][4];
+  if (t >= M) return;
+  // route positions of this token, one per lane
+  const int my_pos = lane < topk ? __ldg(route_pos + static_cast<int64_t>(t) * topk + lane) : -1;
+  if (threadIdx.x == 0) MOE_TL_AFTER(3, 3, my_pos);
+  if (A16) {
+    for (int j = 0; j < topk; ++j) {
+      const int p = __shfl_sync(0xffffffffu, my_pos, j);
+      if (p < 0 || !in) continue;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(act) +
+                                            static_cast<int64_t>(p) * H + b * 32);
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int b = b0 + i * 32 + lane;
-        if (b < nblk) {
-          const uint4* src = reinterpret_cast<const uint4*>(xr + b * 32);
+      for (int q = 0; q < 4; ++q) dst[q] = raw[q];
+    }
+  } else {
+    uint32_t c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    uint32_t sb = 0;
+    if (in) {
+      float v[32];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) raw[i][q] = __ldg(src + q);
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[q * 8 + 2 * j] = __uint_as_float(w4[j] << 16);
+          v[q * 8 + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
         }
       }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int b = b0 + i * 32 + lane;
-        const bool in = b < nblk;
-        if (A16) {
-          for (int j = 0; j < topk; ++j) {
-            const int p = __shfl_sync(0xffffffffu, my_pos, j);
-            if (p < 0 || !in) continue;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(act) +
-                                                  static_cast<int64_t>(p) * H + b * 32);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = raw[i][q];
-          }
-        } else {
-          float v[32];
-          uint32_t c[8];
-          uint8_t sb = 0;
-          if (in) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t w4[4] = {raw[i][q].x, raw[i][q].y, raw[i][q].z, raw[i][q].w};
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                v[q * 8 + 2 * j] = __uint_as_float(w4[j] << 16);
-                v[q * 8 + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
-              }
-            }
-            sb = quant_block32(v, c);
-          }
-          if (threadIdx.x == 0 && i == 0) MOE_TL_AFTER(3, 4, sb);
-          for (int j = 0; j < topk; ++j) {
-            const int p = __shfl_sync(0xffffffffu, my_pos, j);
-            if (p < 0 || !in) continue;
-            store_codes32(static_cast<uint8_t*>(act) + static_cast<int64_t>(p) * H + b * 32, c);
-            const int blk = p / bm, rr = p % bm;
-            const int64_t atom = (static_cast<int64_t>(blk) * nslab + b / 4) * atoms + rr / 128;
-            act_sf[atom * 512 + sf_atom_off(rr & 127, b & 3)] = sb;
-          }
-        }
+      sb = quant_block32(v, c);
+    }
+    // the four blocks of a 128-column slab sit in lanes 4s .. 4s+3
+    const uint32_t word = sb | (__shfl_down_sync(0xffffffffu, sb, 1) << 8) |
+                          (__shfl_down_sync(0xffffffffu, sb, 2) << 16) |
+                          (__shfl_down_sync(0xffffffffu, sb, 3) << 24);
+    if (threadIdx.x == 0) MOE_TL_AFTER(3, 4, word);
+    const int atoms = (bm + 127) / 128;
+    const int nslab = H / 128;
+    for (int j = 0; j < topk; ++j) {
+      const int p = __shfl_sync(0xffffffffu, my_pos, j);
+      if (p < 0 || !in) continue;
+      store_codes32(static_cast<uint8_t*>(act) + static_cast<int64_t>(p) * H + b * 32, c);
+      if ((lane & 3) == 0) {
+        const int blk = p / bm, rr = p % bm;
+        const int64_t atom = (static_cast<int64_t>(blk) * nslab + b / 4) * atoms + rr / 128;
+        *reinterpret_cast<uint32_t*>(act_sf + atom * 512 + sf_atom_off(rr & 127, 0)) = word;
       }
     }
   }
-  if (threadIdx.x == 0) MOE_TL(3, 5);
-#ifdef MOE_TIMELINE
-  __syncthreads();
-#endif
-  if (threadIdx.x == 0) MOE_TL(3, 7);
+  if (threadIdx.x == 0) {
+    MOE_TL(3, 5);
+    MOE_TL(3, 7);
+  }
 }
 
 __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* __restrict__ scale,
@@ -236,7 +235,9 @@ cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, i
                               const int32_t* route_pos, void* act, uint8_t* act_sf, float* acc,
                               cudaStream_t s) {
   if (topk > 32) return cudaErrorInvalidValue;
-  const int grid = (M + 7) / 8 > 0 ? (M + 7) / 8 : 1;
+  // one warp per (token, 1024-column chunk), 8 warps per CTA
+  const int64_t warps = static_cast<int64_t>(M) * ((H / 32 + 31) / 32);
+  const int grid = warps > 0 ? static_cast<int>((warps + 7) / 8) : 1;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
