@@ -41,6 +41,20 @@ MOE_TL_DEFINE(moe_tl_dump_bf16)
 namespace moe {
 namespace {
 
+#ifdef MOE_WAIT_STATS
+// Experiment builds only: per-CTA cycles each role spent at its barriers,
+// [cta][stage-1][slot]: 0 producer/empty, 1 MMA/full, 2 MMA/a_full,
+// 3 MMA/acc_empty, 4 converter/full, 5 converter/a_empty, 6 converter busy,
+// 7 epilogue/acc_full, 8 kernel cycles.
+__device__ long long g_ws16[512][2][16];
+#define WS_T0() const long long _wt0 = clock64()
+#define WS_ADD(i) atomicAdd(reinterpret_cast<unsigned long long*>(&g_ws16[blockIdx.x & 511][a.stage - 1][(i)]), \
+                            static_cast<unsigned long long>(clock64() - _wt0))
+#else
+#define WS_T0()
+#define WS_ADD(i)
+#endif
+
 constexpr int kTileN = 128;   // weight rows per tile (MMA M)
 constexpr int kTileK = 128;   // K per stage = one prepacked 8 KB weight tile
 constexpr int kMmaK = 16;     // K per tcgen05.mma kind::f16
@@ -71,7 +85,11 @@ __host__ __device__ constexpr int pow2_cols(int c) {
 template <int BN>
 struct Cfg16 {
   // Small route blocks run two CTAs per SM so that two MMA issuers and two
-  // converter groups share the SM; their TMEM halves hold 3 weight slots each.
+  // converter groups share the SM. The dequantised-weight slots in TMEM are
+  // the shared-memory stages (slot = stage), so one commit per k-block frees
+  // both: the converter writes slot s only after the stage's new TMA data
+  // landed, and the producer issued those loads only after the MMA that read
+  // slot s had committed. The ring depth is therefore bounded by TMEM.
   static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
   static constexpr int kConvWarps = kCtasPerSm == 2 ? 4 : 8;
   static constexpr int kThreads = 192 + 32 * kConvWarps;
@@ -81,8 +99,8 @@ struct Cfg16 {
   static constexpr int kBBytes = 2 * kBAtomBytes;
   // stage layout: B atoms, raw FP4 tile (64-byte swizzled), scale atom
   static constexpr int kStageBytes = (kBBytes + kRawBytes + kSfBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN == 16 ? 5 : BN == 32 ? 4 : BN == 64 ? 6 : BN == 128 ? 4 : 2;
-  static constexpr int kASlots = kCtasPerSm == 2 ? 3 : 4;
+  static constexpr int kStages = BN <= 32 ? 3 : BN == 64 ? 6 : BN == 128 ? 4 : 2;
+  static constexpr int kASlots = kStages;
   static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
   static constexpr int kAccCol0 = kASlots * kACols;
   static constexpr int kTmemCols = pow2_cols(kAccCol0 + kAccBufs * BN);
@@ -140,13 +158,16 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token / -1 pad
   float* s_w = reinterpret_cast<float*>(s_tok + 256);             // [BN] routing weight
   __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
-  __shared__ uint64_t a_full[C::kASlots], a_empty[C::kASlots];
+  __shared__ uint64_t a_full[C::kASlots];
   __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef MOE_WAIT_STATS
+  const long long _k0 = clock64();
+#endif
   pdl_launch_dependents();
   if (threadIdx.x == 0) MOE_TL(3 + a.stage, 0);
   const int total_tiles = a.num_blocks * a.n_tiles;
@@ -159,7 +180,6 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     }
     for (int j = 0; j < C::kASlots; ++j) {
       mbar_init(&a_full[j], C::kConvWarps);
-      mbar_init(&a_empty[j], 1);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -223,7 +243,9 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       while (cur.valid && !abort_flag) {
         const int64_t tile0 = (static_cast<int64_t>(cur.e) * a.n_tiles + cur.n_tile) * kblocks;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
+          bool ok;
+          { WS_T0(); ok = mbar_wait(&empty_bar[stage], phase ^ 1, a.status); WS_ADD(0); }
+          if (!ok) { abort_flag = 1; break; }
           uint8_t* sb = stage_ptr(stage);
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
 #ifdef MOE_TIMELINE
@@ -246,8 +268,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
     if (lane == 0) {
-      int stage = 0, slot = 0;
-      uint32_t phase = 0, aphase = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       int local = 0;
 #ifdef MOE_TIMELINE
       int tl_mma = 1;
@@ -259,18 +281,22 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
         ++local;
-        if (!mbar_wait(&acc_empty[ab], acc_phase ^ 1, a.status)) { abort_flag = 1; break; }
+        bool ok0;
+        { WS_T0(); ok0 = mbar_wait(&acc_empty[ab], acc_phase ^ 1, a.status); WS_ADD(3); }
+        if (!ok0) { abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + C::kAccCol0 + ab * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, a.status) ||
-              !mbar_wait(&a_full[slot], aphase, a.status)) { abort_flag = 1; break; }
+          bool ok1, ok2;
+          { WS_T0(); ok1 = mbar_wait(&full_bar[stage], phase, a.status); WS_ADD(1); }
+          { WS_T0(); ok2 = ok1 && mbar_wait(&a_full[stage], phase, a.status); WS_ADD(2); }
+          if (!ok2) { abort_flag = 1; break; }
 #ifdef MOE_TIMELINE
           if (tl_mma) { MOE_TL(3 + a.stage, 3); tl_mma = 0; }
 #endif
           tc_fence_after();
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (C::kStageBytes >> 4);
-          const uint32_t a_tmem = tmem + slot * kACols;
+          const uint32_t a_tmem = tmem + stage * kACols;
 #pragma unroll
           for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
             // B: atom h of the stage, then 32 bytes (2 descriptor units) per MMA;
@@ -279,10 +305,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
             mma_f16_tmem_a(d_tmem, a_tmem + kk * (kMmaK / 2),
                            bd + h * (C::kBAtomBytes >> 4) + off, idesc, (kb | kk) != 0);
           }
-          tc_commit(&empty_bar[stage]);
-          tc_commit(&a_empty[slot]);
+          tc_commit(&empty_bar[stage]);         // frees the smem stage and its TMEM slot
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-          if (++slot == C::kASlots) { slot = 0; aphase ^= 1; }
         }
         tc_commit(&acc_full[ab]);
       }
@@ -300,14 +324,26 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     const int sf_off = sf_atom_off(r, 0);                // its 4 scale bytes
     const uint32_t* lut_lane = lut + lane;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    int stage = 0, slot = 0;
-    uint32_t phase = 0, aphase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
     Seq16 seq;
     for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
       bool stop = false;
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (abort_flag || !mbar_wait(&full_bar[stage], phase, a.status) ||
-            !mbar_wait(&a_empty[slot], aphase ^ 1, a.status)) {
+        bool okc1 = !abort_flag, okc2;
+#ifdef MOE_WAIT_STATS
+        const bool rep = threadIdx.x == 192;
+#endif
+        { WS_T0(); okc1 = okc1 && mbar_wait(&full_bar[stage], phase, a.status);
+#ifdef MOE_WAIT_STATS
+          if (rep) WS_ADD(4);
+#endif
+        }
+        okc2 = okc1;   // slot `stage` is free once the stage's data has landed
+#ifdef MOE_WAIT_STATS
+        const long long _cb0 = clock64();
+#endif
+        if (!okc2) {
           abort_flag = 1; stop = true; break;
         }
         tc_fence_after();
@@ -332,14 +368,18 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
                 out[cc * 16 + wi * 4 + b] = bf16x2_mul(lut_lane[idx * 32], sc);
               }
           }
-          tmem_st_32x32b_x32(t_row + slot * kACols + h * 32, out);
+          tmem_st_32x32b_x32(t_row + stage * kACols + h * 32, out);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[slot]);
+        if (lane == 0) mbar_arrive(&a_full[stage]);
+#ifdef MOE_WAIT_STATS
+        if (rep)
+          atomicAdd(reinterpret_cast<unsigned long long*>(&g_ws16[blockIdx.x & 511][a.stage - 1][6]),
+                    static_cast<unsigned long long>(clock64() - _cb0));
+#endif
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-        if (++slot == C::kASlots) { slot = 0; aphase ^= 1; }
       }
       if (stop) break;
     }
@@ -369,7 +409,13 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         }
         named_bar_sync(1, 128);
       }
-      if (abort_flag || !mbar_wait(&acc_full[ab], acc_phase, a.status)) { abort_flag = 1; break; }
+      bool oke = !abort_flag;
+      { WS_T0(); oke = oke && mbar_wait(&acc_full[ab], acc_phase, a.status);
+#ifdef MOE_WAIT_STATS
+        if (threadIdx.x == 64) WS_ADD(7);
+#endif
+      }
+      if (!oke) { abort_flag = 1; break; }
       tc_fence_after();
       const uint32_t d_tmem =
           tmem + C::kAccCol0 + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
@@ -452,6 +498,11 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+#ifdef MOE_WAIT_STATS
+  if (threadIdx.x == 0)
+    atomicAdd(reinterpret_cast<unsigned long long*>(&g_ws16[blockIdx.x & 511][a.stage - 1][8]),
+              static_cast<unsigned long long>(clock64() - _k0));
+#endif
   if (threadIdx.x == 0) {
     MOE_TL(3 + a.stage, 7);
   }
@@ -539,3 +590,13 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
 }
 
 }  // namespace moe
+
+#ifdef MOE_WAIT_STATS
+extern "C" void moe_debug_wait_stats16(long long* host_out, int reset) {
+  cudaMemcpyFromSymbol(host_out, moe::g_ws16, sizeof(moe::g_ws16));
+  if (reset) {
+    static long long zeros[512][2][16] = {};
+    cudaMemcpyToSymbol(moe::g_ws16, zeros, sizeof(zeros));
+  }
+}
+#endif
