@@ -9,6 +9,8 @@ namespace moe {
 
 constexpr int kMaxExperts = 512;   // expert ids fit 9 bits (route sort)
 constexpr int kMaxTopk = 16;
+// Up to this many routes the call's front (sort + gather) is one launch.
+constexpr int kFrontMaxRoutes = 256;
 
 // Byte offset of (row r, 32-block i) inside a 128-row x 4-block scale atom:
 // rows are split into four 32-row groups that sit side by side in each

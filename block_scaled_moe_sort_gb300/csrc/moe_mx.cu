@@ -155,17 +155,29 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   float* acc = reinterpret_cast<float*>(base + L.acc_off);
   const int R = M * topk;
 
-  prof_mark(0, true, s);
-  int32_t* sort_scratch = reinterpret_cast<int32_t*>(base + L.sort_scratch_off);
-  cudaError_t e = launch_sort(ids, wts, R, E, L.block_m, L.p_max, sorted_route, sorted_w,
-                              block_expert, expert_off, num_padded, route_pos, status,
-                              sort_scratch, s);
-  if (e != cudaSuccess) return from_cuda(e);
-  prof_mark(0, false, s);
-  prof_mark(1, true, s);
-  e = launch_gather_act(a16, x, M, H, topk, L.block_m, route_pos, act, act_sf, acc, s);
-  if (e != cudaSuccess) return from_cuda(e);
-  prof_mark(1, false, s);
+  cudaError_t e;
+  if (R <= kFrontMaxRoutes) {
+    // decode: sort and gather in one launch (profiled as the sort slot)
+    prof_mark(0, true, s);
+    e = launch_front_tiny(a16, x, ids, wts, M, H, topk, E, L.block_m, L.p_max, sorted_route,
+                          sorted_w, block_expert, expert_off, num_padded, route_pos, status, act,
+                          act_sf, acc, nullptr, 0, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    prof_mark(0, false, s);
+    prof_mark(1, true, s);
+    prof_mark(1, false, s);
+  } else {
+    prof_mark(0, true, s);
+    int32_t* sort_scratch = reinterpret_cast<int32_t*>(base + L.sort_scratch_off);
+    e = launch_sort(ids, wts, R, E, L.block_m, L.p_max, sorted_route, sorted_w, block_expert,
+                    expert_off, num_padded, route_pos, status, sort_scratch, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    prof_mark(0, false, s);
+    prof_mark(1, true, s);
+    e = launch_gather_act(a16, x, M, H, topk, L.block_m, route_pos, act, act_sf, acc, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    prof_mark(1, false, s);
+  }
   GemmArgs g{};
   g.a16 = a16;
   g.M = M; g.H = H; g.Ip = Ip; g.E = E; g.topk = topk; g.bm = L.block_m;
