@@ -39,7 +39,8 @@ class MoeWsLayout(ctypes.Structure):
                 ("block_expert_off", _c_int64), ("route_pos_off", _c_int64),
                 ("sort_scratch_off", _c_int64),
                 ("act_off", _c_int64), ("act_sf_off", _c_int64), ("inter_off", _c_int64),
-                ("inter_sf_off", _c_int64), ("acc_off", _c_int64), ("total_bytes", _c_int64)]
+                ("inter_sf_off", _c_int64), ("acc_off", _c_int64), ("split_part_off", _c_int64),
+                ("split_cnt_off", _c_int64), ("total_bytes", _c_int64)]
 
 
 _SIGS = {

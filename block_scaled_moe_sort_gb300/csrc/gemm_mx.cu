@@ -31,6 +31,7 @@
 // so launch shapes depend only on host-known sizes (graph capturable).
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include "common.cuh"
@@ -79,6 +80,10 @@ struct MxArgs {
   uint8_t* inter_sf;     // stage 1 out: atoms [blocks][Ip/128][na][512]
   float* acc;            // stage 2 out: [M, H]
   int32_t* status;
+  // stage-1 tail split (decode): FP32 partial sums [kSplitSlots][BN][128] and
+  // arrival counters [kSplitSlots], zero at the start of the call
+  float* split_part;
+  int32_t* split_cnt;
 };
 
 template <int BN>
@@ -116,13 +121,14 @@ struct Cfg {
   static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
 };
 
-using Seq = TileSeq<MxArgs>;
 
-template <int BN>
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const MxArgs a) {
   using C = Cfg<BN>;
+  // SPLIT: stage 1 with the tail split (SplitSeq units, partial-sum epilogue)
+  using Seq = typename std::conditional<SPLIT, SplitSeq<MxArgs>, TileSeq<MxArgs>>::type;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic so that the
   // compiler keeps every access below in the shared state space
@@ -136,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
   __shared__ uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ int split_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       uint32_t phase = 0;
       uint8_t* sbase = stages;
       Seq cur;
-      cur.init(a, total_tiles, P, BN);
+      seq_init(cur, a, total_tiles, P, BN, kblocks);
 #ifdef MOE_TIMELINE
       int tl_first = 1;
 #endif
@@ -200,25 +207,27 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       const uint8_t* pf_w = nullptr;
       auto pf_tile = [&]() {
         pf_w = a.w_base + (static_cast<int64_t>(pf.e) * a.n_tiles + pf.n_tile) * kblocks * kWTile;
+        pf_kb = seq_kb0(pf);
       };
       if (pf.valid) pf_tile();
       auto pf_step = [&]() {
         if (!pf.valid) return;
         bulk_prefetch_l2(pf_w + static_cast<int64_t>(pf_kb) * kWTile, kWTile);
-        if (++pf_kb == kblocks) {
-          pf_kb = 0;
-          pf.next(a, total_tiles, P, BN);
+        if (++pf_kb == seq_kb1(pf, kblocks)) {
+          seq_next(pf, a, total_tiles, P, BN);
           if (pf.valid) pf_tile();
         }
       };
       for (int i = 0; i < kPrefetch; ++i) pf_step();
       while (cur.valid && !abort_flag) {
         const int64_t wtile = static_cast<int64_t>(cur.e) * a.n_tiles + cur.n_tile;
-        int row_a = static_cast<int>(wtile * kblocks * kTileN);
-        const uint8_t* sfa = a.sfa + wtile * kblocks * 512;
-        const uint8_t* sfb = a.sfb + static_cast<int64_t>(cur.m_blk) * kblocks * C::kNa * 512;
+        const int kb_begin = seq_kb0(cur), kb_end = seq_kb1(cur, kblocks);
+        int row_a = static_cast<int>((wtile * kblocks + kb_begin) * kTileN);
+        const uint8_t* sfa = a.sfa + (wtile * kblocks + kb_begin) * 512;
+        const uint8_t* sfb =
+            a.sfb + (static_cast<int64_t>(cur.m_blk) * kblocks + kb_begin) * C::kNa * 512;
         const int row_b = cur.m_blk * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           {
             WAIT_T0();
             if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             sbase += C::kStageBytes;
           }
         }
-        cur.next(a, total_tiles, P, BN);
+        seq_next(cur, a, total_tiles, P, BN);
       }
     }
   } else if (warp == 1) {
@@ -269,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
 #ifdef MOE_TIMELINE
       int tl_mma = 1;
 #endif
-      for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
+      for (seq_init(seq, a, total_tiles, P, BN, kblocks); seq.valid && !abort_flag;
+           seq_next(seq, a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
         ++local;
@@ -280,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + ab * C::kAccCols;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const int kb_begin = seq_kb0(seq), kb_end = seq_kb1(seq, kblocks);
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           {
             WAIT_T0();
             if (!mbar_wait(&full_bar[stage], phase, a.status)) { abort_flag = 1; break; }
@@ -299,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
           for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
             mma_mxf8f6f4(d_tmem + (kk % C::kSplit) * BN, ad + 2 * kk, bd + 2 * kk,
                          idesc_mx(5, 0, kTileN, BN, kk, kk), sf_tmem, sf_tmem + 4,
-                         kb > 0 || kk >= C::kSplit);
+                         kb > kb_begin || kk >= C::kSplit);
           }
           tc_commit(&empty_bar[stage]);
           if (++stage == C::kStages) {
@@ -327,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     const int R = a.M * a.topk;
     int local = 0;
     Seq seq;
-    for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
+    for (seq_init(seq, a, total_tiles, P, BN, kblocks); seq.valid;
+         seq_next(seq, a, total_tiles, P, BN)) {
       const int m_blk = seq.m_blk, n_tile = seq.n_tile;
       const int ab = local % C::kAccBufs;
       const uint32_t acc_phase = (local / C::kAccBufs) & 1;
@@ -357,8 +369,57 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       const uint32_t d_tmem = tmem + ab * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
       constexpr int kChunk = BN < 32 ? BN : 32;
+      // Tail split: a K range of a split tile adds its partial sums to the
+      // tile's slot (feature row fastest: a warp adds 128 contiguous bytes),
+      // releases the accumulator and counts itself in; the range that arrives
+      // last reads the complete sums back from L2 and runs the epilogue.
+      float* part = nullptr;
+      if constexpr (SPLIT) {
+        if (seq.slot >= 0) {
+          part = a.split_part + static_cast<int64_t>(seq.slot) * BN * 128;
+          for (int c0 = 0; c0 < BN; c0 += kChunk) {
+            float v[32];
+#pragma unroll
+            for (int sp = 0; sp < C::kSplit; ++sp) {
+              uint32_t r[32];
+              if constexpr (kChunk == 32) {
+                tmem_ld_32x32b_x32(d_tmem + sp * BN + c0, r);
+              } else {
+                uint32_t r16[16];
+                tmem_ld_32x32b_x16(d_tmem + sp * BN + c0, r16);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = r16[i];
+              }
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < kChunk; ++i)
+                v[i] = sp == 0 ? __uint_as_float(r[i]) : v[i] + __uint_as_float(r[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) atomicAdd(part + (c0 + i) * 128 + row, v[i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ab]);
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (et == 0) split_last = atomicAdd(a.split_cnt + seq.slot, 1) == seq.S - 1;
+          named_bar_sync(1, 128);
+          if (!split_last) continue;
+          __threadfence();
+        }
+      }
       for (int c0 = 0; c0 < BN; c0 += kChunk) {
         float v[32];
+        bool from_part = false;
+        if constexpr (SPLIT) {
+          if (part) {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) v[i] = __ldcg(part + (c0 + i) * 128 + row);
+            from_part = true;
+          }
+        }
+        if (!from_part) {
 #pragma unroll
         for (int sp = 0; sp < C::kSplit; ++sp) {
           uint32_t r[32];
@@ -375,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
           for (int i = 0; i < kChunk; ++i)
             v[i] = sp == 0 ? __uint_as_float(r[i]) : v[i] + __uint_as_float(r[i]);
         }
-        if (a.stage == 1) {
+        }
+        if (SPLIT || a.stage == 1) {
           // Gate (row 2j) and up (row 2j+1) sit in adjacent lanes. Even lanes
           // produce columns [0, half), odd lanes [half, kChunk): one shuffle
           // per column pair, no divergence.
@@ -448,9 +510,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      if (!SPLIT || !part) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      }
 #ifdef MOE_WAIT_STATS
       if (threadIdx.x == 64)
         atomicAdd(reinterpret_cast<unsigned long long*>(&g_wait_stats[blockIdx.x][(a.stage - 1) * 8 + 5]),
@@ -520,13 +584,22 @@ template <int BN>
 cudaError_t plan_bn(const MxArgs& a, int num_sms, GemmPlan* plan) {
   using C = Cfg<BN>;
   static_assert(sizeof(MxArgs) <= sizeof(plan->args), "argument block");
-  const void* fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN>);
+  // the tail-split kernel for stage 1 only where the tiles cannot fill
+  // kSplitMaxWaves waves even at the route count's upper bound (decode)
+  const void* fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, false>);
+  if constexpr (BN <= 32) {
+    if (a.stage == 1 && a.split_part &&
+        static_cast<int64_t>(a.num_blocks) * a.n_tiles < kSplitMaxWaves * num_sms * C::kCtasPerSm)
+      fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, true>);
+  }
   cudaError_t err = ensure_smem_attr(fn, C::kSmem);
   if (err != cudaSuccess) return err;
   const int tiles = a.num_blocks * a.n_tiles;
   const int slots = num_sms * C::kCtasPerSm;
   plan->kernel = fn;
-  plan->grid = tiles < slots ? tiles : slots;
+  // the split kernel spreads the tail tiles over every CTA slot
+  const bool split_kernel = fn != reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, false>);
+  plan->grid = split_kernel || tiles > slots ? slots : tiles;
   plan->threads = kThreads;
   plan->smem = C::kSmem;
   memcpy(plan->args, &a, sizeof(a));
@@ -559,6 +632,8 @@ cudaError_t prepare_gemm_mx(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.inter_sf = g.inter_sf;
   a.acc = g.acc;
   a.status = g.status;
+  a.split_part = g.split_part;
+  a.split_cnt = g.split_cnt;
   plan->grid = 0;
   if (a.num_blocks == 0) return cudaSuccess;
   const uint8_t* w = stage == 1 ? g.w1 : g.w2;

@@ -5,6 +5,7 @@
 // accumulator, i.e. in L2).
 #pragma once
 #include <cstdint>
+#include "common.cuh"
 
 namespace moe {
 
@@ -53,5 +54,93 @@ struct TileSeq {
     ne = nvalid ? __ldg(a.block_expert + nm) : -1;
   }
 };
+
+
+// ------------------------------------------------------ stage-1 tail split
+// With few tiles (decode) the last, partial wave of stage-1 tiles leaves most
+// CTAs idle. SplitSeq walks stage-1 work units instead: with T tiles on a grid
+// of G CTAs, W = T / G whole waves and r = T - W * G tiles left over, the r
+// tiles are split into S = min(G / r, kblocks, kSplitMaxParts) K ranges when
+// W < kSplitMaxWaves. Units [0, W * G) are whole tiles; unit W * G + v is K
+// range v % S of tile W * G + v / S, whose partial sums go to slot v / S of
+// the split buffer (the range that finishes last runs the epilogue). Stage-1
+// tiles are route-block major, so the tiles that hold routes are the first
+// (P / bn) * n_tiles.
+constexpr int kSplitMaxWaves = 2;
+constexpr int kSplitMaxParts = 8;
+
+template <class Args>
+struct SplitSeq {
+  int t, m_blk, n_tile, e, kb0, kb1, slot;
+  bool valid;
+  int nt, nm, nn, ne, nkb0, nkb1, nslot;
+  bool nvalid;
+  int wg, S, U, kblocks;
+
+  __device__ __forceinline__ bool locate(int u, int& m, int& n, int& k0, int& k1, int& sl,
+                                         const Args& a) const {
+    if (u >= U) return false;
+    int tt;
+    if (u < wg) {
+      tt = u; k0 = 0; k1 = kblocks; sl = -1;
+    } else {
+      const int v = u - wg, part = v % S;
+      tt = wg + v / S;
+      k0 = part * kblocks / S;
+      k1 = (part + 1) * kblocks / S;
+      sl = v / S;
+    }
+    m = tt / a.n_tiles;
+    n = tt % a.n_tiles;
+    return true;
+  }
+  __device__ __forceinline__ void init(const Args& a, int P, int bn, int kb) {
+    kblocks = kb;
+    const int T = (P / bn) * a.n_tiles;
+    const int G = gridDim.x;
+    const int W = T / G, r = T - W * G;
+    int parts = 1;
+    if (W < kSplitMaxWaves && r > 0 && r <= kSplitSlots) parts = min(min(G / r, kblocks), kSplitMaxParts);
+    if (parts > 1) { S = parts; wg = W * G; U = wg + r * parts; } else { S = 1; wg = T; U = T; }
+    t = blockIdx.x;
+    valid = locate(t, m_blk, n_tile, kb0, kb1, slot, a);
+    e = valid ? __ldg(a.block_expert + m_blk) : -1;
+    nt = t + gridDim.x;
+    nvalid = valid && locate(nt, nm, nn, nkb0, nkb1, nslot, a);
+    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+  }
+  __device__ __forceinline__ void next(const Args& a) {
+    t = nt; m_blk = nm; n_tile = nn; e = ne; kb0 = nkb0; kb1 = nkb1; slot = nslot;
+    valid = nvalid;
+    nt = t + gridDim.x;
+    nvalid = valid && locate(nt, nm, nn, nkb0, nkb1, nslot, a);
+    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+  }
+};
+
+
+// Uniform access for the kernels: a TileSeq unit always covers the whole K
+// range (constant 0 / kblocks, so kernels using it compile as before).
+template <class Args>
+__device__ __forceinline__ void seq_init(TileSeq<Args>& q, const Args& a, int total, int P, int bn,
+                                         int) { q.init(a, total, P, bn); }
+template <class Args>
+__device__ __forceinline__ void seq_init(SplitSeq<Args>& q, const Args& a, int, int P, int bn,
+                                         int kb) { q.init(a, P, bn, kb); }
+template <class Args>
+__device__ __forceinline__ void seq_next(TileSeq<Args>& q, const Args& a, int total, int P,
+                                         int bn) { q.next(a, total, P, bn); }
+template <class Args>
+__device__ __forceinline__ void seq_next(SplitSeq<Args>& q, const Args& a, int, int, int) {
+  q.next(a);
+}
+template <class Args>
+__device__ __forceinline__ int seq_kb0(const TileSeq<Args>&) { return 0; }
+template <class Args>
+__device__ __forceinline__ int seq_kb0(const SplitSeq<Args>& q) { return q.kb0; }
+template <class Args>
+__device__ __forceinline__ int seq_kb1(const TileSeq<Args>&, int kblocks) { return kblocks; }
+template <class Args>
+__device__ __forceinline__ int seq_kb1(const SplitSeq<Args>& q, int) { return q.kb1; }
 
 }  // namespace moe

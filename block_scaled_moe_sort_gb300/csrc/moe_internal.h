@@ -36,10 +36,10 @@ cudaError_t launch_front_tiny(bool a16, const void* x, const int32_t* ids, const
 
 // Writes each token's activation row to the sorted position of each of its
 // routes (quantised to FP8 with scale atoms for a8w4, as BF16 for a16w4) and
-// zeroes the FP32 accumulator [M, H].
+// zeroes the FP32 accumulator [M, H] and zero2_bytes (a multiple of 16) at zero2.
 cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, int bm,
                               const int32_t* route_pos, void* act, uint8_t* act_sf, float* acc,
-                              cudaStream_t s);
+                              void* zero2, int64_t zero2_bytes, cudaStream_t s);
 
 cudaError_t launch_finalize(const float* acc, int64_t n, void* out, cudaStream_t s);
 
@@ -60,6 +60,8 @@ struct GemmArgs {
   void* inter;          // [p_max, Ip]
   uint8_t* inter_sf;
   float* acc;           // [M, H]
+  float* split_part;    // stage-1 tail split: [kSplitSlots][block_m][128] FP32, zeroed per call
+  int32_t* split_cnt;   // [kSplitSlots], zeroed per call
   int32_t* status;
 };
 

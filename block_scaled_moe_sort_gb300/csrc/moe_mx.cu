@@ -91,6 +91,10 @@ void build_layout(int M, int H, int Ip, int E, int topk, bool a16, moe_ws_layout
   L->inter_off = take(pm * Ip * (a16 ? 2 : 1));
   L->inter_sf_off = take(a16 ? 0 : nblk * (Ip / 128) * atoms * 512);
   L->acc_off = take(static_cast<int64_t>(M) * H * 4);
+  // stage-1 tail split buffers (a8w4 decode block sizes only)
+  const bool split = !a16 && bm <= 32;
+  L->split_part_off = take(split ? static_cast<int64_t>(kSplitSlots) * bm * 128 * 4 : 0);
+  L->split_cnt_off = take(split ? kSplitSlots * 4 : 0);
   L->total_bytes = o;
 }
 
@@ -154,6 +158,11 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   uint8_t* inter_sf = base + L.inter_sf_off;
   float* acc = reinterpret_cast<float*>(base + L.acc_off);
   const int R = M * topk;
+  const bool split = L.split_cnt_off > L.split_part_off;
+  float* split_part = split ? reinterpret_cast<float*>(base + L.split_part_off) : nullptr;
+  int32_t* split_cnt = split ? reinterpret_cast<int32_t*>(base + L.split_cnt_off) : nullptr;
+  // the split buffers are zeroed with the accumulator (one contiguous region)
+  const int64_t split_bytes = split ? L.split_cnt_off + kSplitSlots * 4 - L.split_part_off : 0;
 
   cudaError_t e;
   if (R <= kFrontMaxRoutes) {
@@ -161,7 +170,7 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
     prof_mark(0, true, s);
     e = launch_front_tiny(a16, x, ids, wts, M, H, topk, E, L.block_m, L.p_max, sorted_route,
                           sorted_w, block_expert, expert_off, num_padded, route_pos, status, act,
-                          act_sf, acc, nullptr, 0, s);
+                          act_sf, acc, split_part, split_bytes, s);
     if (e != cudaSuccess) return from_cuda(e);
     prof_mark(0, false, s);
     prof_mark(1, true, s);
@@ -174,7 +183,8 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
     if (e != cudaSuccess) return from_cuda(e);
     prof_mark(0, false, s);
     prof_mark(1, true, s);
-    e = launch_gather_act(a16, x, M, H, topk, L.block_m, route_pos, act, act_sf, acc, s);
+    e = launch_gather_act(a16, x, M, H, topk, L.block_m, route_pos, act, act_sf, acc, split_part,
+                          split_bytes, s);
     if (e != cudaSuccess) return from_cuda(e);
     prof_mark(1, false, s);
   }
@@ -186,6 +196,8 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   g.num_padded = num_padded;
   g.w1 = w1; g.w1s = w1s; g.w2 = w2; g.w2s = w2s;
   g.act = act; g.act_sf = act_sf; g.inter = inter; g.inter_sf = inter_sf; g.acc = acc;
+  g.split_part = split_part;
+  g.split_cnt = split_cnt;
   g.status = status;
   GemmPlan plan1, plan2;
   e = a16 ? prepare_gemm_bf16w4(1, g, &plan1) : prepare_gemm_mx(1, g, &plan1);

@@ -66,12 +66,13 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
 // aligned 4-byte word of the route block's MMA scale atom (single bytes
 // scattered over the atoms were partial-sector writes that stalled the
 // stores). Rows of pad entries are never written: their GEMM columns are
-// discarded by both epilogues. The CTAs also zero the FP32 accumulator.
+// discarded by both epilogues. The CTAs also zero the FP32 accumulator and
+// zero2 (the stage-1 split buffers), before waiting on the sort.
 template <bool A16>
 __global__ void __launch_bounds__(256) gather_act_kernel(
     const __nv_bfloat16* __restrict__ x, int M, int H, int topk, int bm,
     const int32_t* __restrict__ route_pos, void* __restrict__ act, uint8_t* __restrict__ act_sf,
-    float* __restrict__ acc) {
+    float* __restrict__ acc, float4* __restrict__ zero2, int64_t zero2_n4) {
   const int lane = threadIdx.x & 31;
   const int nblk = H / 32;
   const int chunks = (nblk + 31) / 32;
@@ -89,6 +90,9 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += stride)
       a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero2_n4;
+         i += stride)
+      zero2[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   uint4 raw[4];
   if (in) {
@@ -403,11 +407,18 @@ cudaError_t launch_quant_act(const void* x, int M, int K, int ldx, uint8_t* q, u
 
 cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, int bm,
                               const int32_t* route_pos, void* act, uint8_t* act_sf, float* acc,
-                              cudaStream_t s) {
+                              void* zero2, int64_t zero2_bytes, cudaStream_t s) {
   if (topk > 32) return cudaErrorInvalidValue;
-  // one warp per (token, 1024-column chunk), 8 warps per CTA
+  // one warp per (token, 1024-column chunk), 8 warps per CTA; at least enough
+  // CTAs that the zeroing (32 KB per CTA) finishes while the sort runs
   const int64_t warps = static_cast<int64_t>(M) * ((H / 32 + 31) / 32);
-  const int grid = warps > 0 ? static_cast<int>((warps + 7) / 8) : 1;
+  const int64_t zero_bytes = static_cast<int64_t>(M) * H * 4 + zero2_bytes;
+  int64_t g = (warps + 7) / 8;
+  const int64_t gz = (zero_bytes + 32767) / 32768;
+  if (gz > g) g = gz < 152 * 8 ? gz : 152 * 8;
+  const int grid = g > 0 ? static_cast<int>(g) : 1;
+  float4* z2 = static_cast<float4*>(zero2);
+  const int64_t z2n = zero2 ? zero2_bytes / 16 : 0;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -420,9 +431,9 @@ cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, i
   cfg.numAttrs = 1;
   if (a16)
     return cudaLaunchKernelEx(&cfg, gather_act_kernel<true>, xb, M, H, topk, bm, route_pos, act,
-                              act_sf, acc);
+                              act_sf, acc, z2, z2n);
   return cudaLaunchKernelEx(&cfg, gather_act_kernel<false>, xb, M, H, topk, bm, route_pos, act,
-                            act_sf, acc);
+                            act_sf, acc, z2, z2n);
 }
 
 cudaError_t launch_front_tiny(bool a16, const void* x, const int32_t* ids, const float* wts, int M,

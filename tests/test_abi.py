@@ -63,7 +63,7 @@ def test_workspace_size_and_layout(L):
         offs = [lay[k] for k in ("status_off", "expert_off_off", "sorted_route_off",
                                  "sorted_w_off", "block_expert_off", "route_pos_off",
                                  "sort_scratch_off", "act_off",
-                                 "inter_off", "acc_off")]
+                                 "inter_off", "acc_off", "split_part_off", "split_cnt_off")]
         assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
         assert lay["block_m"] in (16, 32, 64, 128, 256)
         assert lay["p_max"] % lay["block_m"] == 0
