@@ -491,6 +491,17 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
     if (threadIdx.x == 64) MOE_TL(3 + a.stage, 5);
+    if (a.stage == 1) {
+      // Zero this CTA's share of the FP32 accumulator that stage 2 reduces
+      // into, after this CTA's last tile: at decode sizes the lines are then
+      // still in L2 when stage 2 starts (which waits for this grid).
+      const int64_t n4 = static_cast<int64_t>(a.M) * a.H / 4;
+      const int64_t per = (n4 + gridDim.x - 1) / gridDim.x;
+      const int64_t lo = static_cast<int64_t>(blockIdx.x) * per;
+      const int64_t hi = lo + per < n4 ? lo + per : n4;
+      float4* a4 = reinterpret_cast<float4*>(a.acc);
+      for (int64_t i = lo + et; i < hi; i += 128) a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -66,8 +66,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __nv_bfloat16* __r
 // aligned 4-byte word of the route block's MMA scale atom (single bytes
 // scattered over the atoms were partial-sector writes that stalled the
 // stores). Rows of pad entries are never written: their GEMM columns are
-// discarded by both epilogues. The CTAs also zero the FP32 accumulator and
-// zero2 (the stage-1 split buffers), before waiting on the sort.
+// discarded by both epilogues. The CTAs also zero zero2 (the stage-1 split
+// buffers) before waiting on the sort.
 template <bool A16>
 __global__ void __launch_bounds__(256) gather_act_kernel(
     const __nv_bfloat16* __restrict__ x, int M, int H, int topk, int bm,
@@ -82,14 +82,10 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
   const bool in = t < M && b < nblk;
   pdl_launch_dependents();
   if (threadIdx.x == 0) MOE_TL(3, 0);
-  // zero the FP32 routing-weighted accumulator (no dependence on the sort)
+  // zero the stage-1 split buffers (the FP32 accumulator is zeroed by the
+  // stage-1 GEMM after its tiles)
   {
-    const int64_t n4 = static_cast<int64_t>(M) * H / 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    float4* a4 = reinterpret_cast<float4*>(acc);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-         i += stride)
-      a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero2_n4;
          i += stride)
       zero2[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -162,7 +158,7 @@ __global__ void __launch_bounds__(256) gather_act_kernel(
 // block_m, ids outside [0, E) dropped: the moe_sort layout), CTA 0 writes it
 // out, and every CTA writes its share of the route-major activation rows
 // (one warp per token and 1024-column chunk, as gather_act_kernel) and zeroes
-// its share of the accumulator and of zero2.
+// its share of zero2.
 struct FrontArgs {
   const int32_t* ids;
   const float* wts;
@@ -270,13 +266,10 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
     for (int64_t blk = P / a.bm + tid; blk < a.p_max / a.bm; blk += blockDim.x)
       a.block_expert[blk] = -1;
   }
-  // zero the accumulator and zero2 (grid-stride over all CTAs)
+  // zero zero2, the stage-1 split buffers (grid-stride over all CTAs; the
+  // accumulator is zeroed by the stage-1 GEMM after its tiles)
   {
-    const int64_t n4 = static_cast<int64_t>(a.M) * a.H / 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    float4* a4 = reinterpret_cast<float4*>(a.acc);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; i < n4; i += stride)
-      a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; i < a.zero2_n4; i += stride)
       a.zero2[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -412,7 +405,7 @@ cudaError_t launch_gather_act(bool a16, const void* x, int M, int H, int topk, i
   // one warp per (token, 1024-column chunk), 8 warps per CTA; at least enough
   // CTAs that the zeroing (32 KB per CTA) finishes while the sort runs
   const int64_t warps = static_cast<int64_t>(M) * ((H / 32 + 31) / 32);
-  const int64_t zero_bytes = static_cast<int64_t>(M) * H * 4 + zero2_bytes;
+  const int64_t zero_bytes = zero2_bytes;
   int64_t g = (warps + 7) / 8;
   const int64_t gz = (zero_bytes + 32767) / 32768;
   if (gz > g) g = gz < 152 * 8 ? gz : 152 * 8;
@@ -448,7 +441,7 @@ cudaError_t launch_front_tiny(bool a16, const void* x, const int32_t* ids, const
               sorted_route, sorted_w, block_expert, expert_off, num_padded, route_pos, status,
               act, act_sf, acc, static_cast<float4*>(zero2), zero2 ? zero2_bytes / 16 : 0};
   const int64_t warps = static_cast<int64_t>(M) * ((H / 32 + 31) / 32);
-  const int64_t zero_bytes = static_cast<int64_t>(M) * H * 4 + zero2_bytes;
+  const int64_t zero_bytes = zero2_bytes;
   int64_t g = (warps + 7) / 8;
   const int64_t gz = (zero_bytes + 32767) / 32768;
   if (gz > g) g = gz < 152 * 8 ? gz : 152 * 8;
