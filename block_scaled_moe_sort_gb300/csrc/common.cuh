@@ -14,6 +14,19 @@ constexpr int kSplitSlots = 320;
 // Up to this many routes the call's front (sort + gather) is one launch.
 constexpr int kFrontMaxRoutes = 256;
 
+// Stage-2 tile walk: feature tiles per group (route-block major inside a
+// group). Once the intermediate no longer fits comfortably in L2, every
+// feature stripe of a plain feature-major walk re-reads all of it from HBM;
+// a group of G stripes reads it once while the G stripes' FP32 accumulator
+// columns (M x G x 512 bytes) stay resident.
+// Returns log2(G).
+inline int stage2_n_group_log2(int64_t M, int64_t inter_bytes, int n_tiles) {
+  if (inter_bytes <= (int64_t(32) << 20)) return 0;
+  int lg = 0;
+  while (lg < 3 && n_tiles % (2 << lg) == 0 && M * 512 * (2 << lg) <= (int64_t(32) << 20)) ++lg;
+  return lg;
+}
+
 // Byte offset of (row r, 32-block i) inside a 128-row x 4-block scale atom:
 // rows are split into four 32-row groups that sit side by side in each
 // 16-byte line, so a 32-lane x 128-bit TMEM copy places row r's four block

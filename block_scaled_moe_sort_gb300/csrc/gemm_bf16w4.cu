@@ -67,6 +67,7 @@ struct Bf16Args {
   int N, K;
   int n_tiles;
   int num_blocks;
+  int n_group_log2;            // stage 2: log2 of the feature tiles per walk group
   const int32_t* sorted_route;
   const float* sorted_w;
   const int32_t* block_expert;
@@ -567,6 +568,7 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.K = stage == 1 ? g.H : g.Ip;
   a.n_tiles = a.N / kTileN;
   a.num_blocks = static_cast<int>(g.p_max / g.bm);
+  a.n_group_log2 = stage == 1 ? 0 : stage2_n_group_log2(g.M, g.p_max * g.Ip * 2, a.n_tiles);
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
   a.num_padded = g.num_padded;
   a.sfa = stage == 1 ? g.w1s : g.w2s;

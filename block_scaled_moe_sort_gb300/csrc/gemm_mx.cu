@@ -69,6 +69,7 @@ struct MxArgs {
   int N, K;              // weight rows per expert / reduction length
   int n_tiles;           // N / 128
   int num_blocks;        // p_max / block_m
+  int n_group_log2;      // stage 2: log2 of the feature tiles per walk group
   const int32_t* sorted_route;
   const float* sorted_w;
   const int32_t* block_expert;
@@ -497,6 +498,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
               a.inter_sf[atom * 512 + sf_atom_off(rr & 127, ib & 3)] = static_cast<uint8_t>(sb);
             }
           }
+        } else if constexpr (BN >= 64) {
+          // stage 2, large tiles: the chunk's weighted values go through
+          // shared memory route-major (8 routes x 128 features per pass, two
+          // alternating buffers, one barrier per pass), and each warp then adds
+          // whole 512-byte token-row segments with 16-byte vector reductions:
+          // a quarter of the reduction instructions of the register path.
+          const int64_t col0 = static_cast<int64_t>(n_tile) * kTileN + 4 * lane;
+#pragma unroll
+          for (int h = 0; h < kChunk / 8; ++h) {
+            float* buf = epi + (h & 1) * (8 * kTileN);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) buf[i * kTileN + row] = v[h * 8 + i] * s_w[c0 + h * 8 + i];
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int r = quad * 2 + j;
+              const int tok = s_tok[c0 + h * 8 + r];
+              if (tok < 0) continue;
+              const float4 f = reinterpret_cast<const float4*>(buf + r * kTileN)[lane];
+              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(tok) * a.H + col0), f);
+            }
+          }
         } else {
           // stage 2: this thread holds output feature `row` of the tile for
           // the chunk's routes, so a warp adds 32 consecutive features (128
@@ -634,6 +657,7 @@ cudaError_t prepare_gemm_mx(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.K = stage == 1 ? g.H : g.Ip;
   a.n_tiles = a.N / kTileN;
   a.num_blocks = static_cast<int>(g.p_max / g.bm);
+  a.n_group_log2 = stage == 1 ? 0 : stage2_n_group_log2(g.M, g.p_max * g.Ip * 1, a.n_tiles);
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
   a.num_padded = g.num_padded;
   a.sfa = stage == 1 ? g.w1s : g.w2s;

@@ -1,8 +1,9 @@
 // Tile walk shared by the grouped GEMM kernels: a tile is (route block,
 // weight-row tile); stage 1 walks route-block major (the n-tiles of a block
-// reuse its activation rows), stage 2 feature-tile major (the FP32
-// reductions of concurrently running tiles stay in one slice of the
-// accumulator, i.e. in L2).
+// reuse its activation rows), stage 2 in groups of 2^n_group_log2 feature tiles,
+// route-block major inside a group (the FP32 reductions of concurrently
+// running tiles stay in the group's slice of the accumulator, i.e. in L2,
+// and the intermediate is read once per group).
 #pragma once
 #include <cstdint>
 #include "common.cuh"
@@ -15,8 +16,10 @@ __device__ __forceinline__ void tile_coords(int t, const Args& a, int& m_blk, in
     m_blk = t / a.n_tiles;
     n_tile = t % a.n_tiles;
   } else {
-    n_tile = t / a.num_blocks;
-    m_blk = t % a.num_blocks;
+    const int g = t / (a.num_blocks << a.n_group_log2);
+    const int r = t - g * (a.num_blocks << a.n_group_log2);
+    m_blk = r >> a.n_group_log2;
+    n_tile = (g << a.n_group_log2) + (r & ((1 << a.n_group_log2) - 1));
   }
 }
 
