@@ -474,16 +474,45 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           }
+        } else if constexpr (BN >= 64) {
+          // stage 2, large tiles: the chunk's weighted values go through
+          // shared memory route-major (8 routes x 128 features per pass, two
+          // alternating buffers, one barrier per pass), and each warp then adds
+          // whole 512-byte token-row segments with 16-byte vector reductions
+          const int64_t col0 = static_cast<int64_t>(n_tile) * kTileN + 4 * lane;
+#pragma unroll
+          for (int h = 0; h < kChunk / 8; ++h) {
+            float* buf = epi + (h & 1) * (8 * kTileN);
+            const float4 wa = reinterpret_cast<const float4*>(s_w + c0 + h * 8)[0];
+            const float4 wb = reinterpret_cast<const float4*>(s_w + c0 + h * 8)[1];
+            const float wk[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) buf[i * kTileN + row] = v[h * 8 + i] * wk[i];
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int r = quad * 2 + j;
+              const int tok = s_tok[c0 + h * 8 + r];
+              if (tok < 0) continue;
+              const float4 f = reinterpret_cast<const float4*>(buf + r * kTileN)[lane];
+              atomicAdd(reinterpret_cast<float4*>(a.acc + static_cast<int64_t>(tok) * a.H + col0), f);
+            }
+          }
         } else {
           // stage 2: this thread holds output feature `row` of the tile for
           // the chunk's routes, so a warp adds 32 consecutive features (128
-          // contiguous bytes of one token row) per reduction, from registers
-          const int64_t col = static_cast<int64_t>(n_tile) * kTileN + row;
+          // contiguous bytes of one token row) per reduction, from registers;
+          // the route info is read four routes per 16-byte broadcast load
+          float* col = a.acc + static_cast<int64_t>(n_tile) * kTileN + row;
 #pragma unroll
-          for (int i = 0; i < kChunk; ++i) {
-            const int tok = s_tok[c0 + i];
-            if (tok < 0) continue;
-            atomicAdd(a.acc + static_cast<int64_t>(tok) * a.H + col, v[i] * s_w[c0 + i]);
+          for (int q = 0; q < kChunk / 4; ++q) {
+            const int4 t4 = reinterpret_cast<const int4*>(s_tok + c0)[q];
+            const float4 w4 = reinterpret_cast<const float4*>(s_w + c0)[q];
+            const int tk[4] = {t4.x, t4.y, t4.z, t4.w};
+            const float wk[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (tk[j] >= 0) atomicAdd(col + static_cast<int64_t>(tk[j]) * a.H, v[4 * q + j] * wk[j]);
           }
         }
       }
