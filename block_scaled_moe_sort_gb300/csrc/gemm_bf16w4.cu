@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // A second cursor runs kPrefetch weight tiles ahead and prefetches them
-    // (contiguous 8 KB blocks) into L2.
+    // (contiguous 8 KB blocks) and their scale atoms into L2.
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
@@ -234,6 +234,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       auto pf_step = [&]() {
         if (!pf.valid) return;
         const int64_t tile = (static_cast<int64_t>(pf.e) * a.n_tiles + pf.n_tile) * kblocks + pf_kb;
+        // with the tile's weight scale atoms (512 B per k-block, contiguous)
+        if (pf_kb == 0) bulk_prefetch_l2(a.sfa + tile * 512, static_cast<uint32_t>(kblocks) * 512);
         bulk_prefetch_l2(a.w + tile * C::kRawBytes, C::kRawBytes);
         if (++pf_kb == kblocks) {
           pf_kb = 0;
