@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_x = policy_evict_last();    // routes: reused across n-tiles
-      constexpr int kPrefetch = 16;
+      // k-blocks the L2 prefetch runs ahead; stage-2 tiles (five k-blocks)
+      // do better with a shorter lead (measured: 8 vs 16 vs 32)
+      const int kPrefetch = a.stage == 2 ? 8 : 16;
       constexpr uint32_t kWTile = kTileN * kTileK / 2;   // 8 KB
       int stage = 0;
       uint32_t phase = 0;
