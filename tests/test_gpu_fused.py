@@ -3,7 +3,8 @@
 Small geometries are compared in full (every token, every intermediate row);
 the pages' geometries (draft, backbone incl. the M31/32/33/255/256/257
 boundary checks and concentrated routing, expert-parallel shard, a16w4
-384-top6 and 385-top7 with the fused shared expert, Zipf prefill stress) are
+384-top6 and 385-top7 with the fused shared expert at decode and prefill
+sizes, Zipf prefill stress) are
 compared on every route of a seeded sample of tokens, at the sizes and in the
 launch configuration the benchmark uses. Workspace and output are poisoned
 (0xFF) before each call, so anything left unwritten shows up.
@@ -87,6 +88,14 @@ def test_expert_parallel_shard(cuda_lib, M):
 def test_a16w4(cuda_lib, name, M):
     layer, case, tok = _config_case(name, M)
     print(compare(case, layer, True, tokens=None if M <= 12 else tok))
+
+
+@pytest.mark.parametrize("name,M", [("a16w4_384", 4096), ("a16w4_385", 16384)])
+def test_a16w4_prefill(cuda_lib, name, M):
+    # route blocks of 64 and 128 rows and the grouped stage-2 tile walk (the
+    # BF16 intermediate is larger than 32 MB) on the a16w4 geometries
+    layer, case, tok = _config_case(name, M)
+    print(compare(case, layer, True, tokens=tok))
 
 
 def test_zipf_prefill_stress(cuda_lib):
