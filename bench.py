@@ -6,7 +6,10 @@ weighted reduction, BF16 output): the DeepSeek-V4.1-Flash TP4 backbone MoE
 at the largest decode bucket of its sweep, M=768 tokens, H=5120,
 I=576 padded to 640, 384 experts, top-6, uniform routing, seeded synthetic
 inputs (AITER #5609 "Add DeepSeek V4.1 Flash TP4 gfx950 MoE tuning",
-Configuration). The other buckets of that sweep are reported under "sweep".
+Configuration). The other buckets of that sweep are reported under "sweep",
+and the gating kernel (router logits -> top-k ids and weights, 384 experts,
+top-6) at the bench M and at M=16384 under "router" (µs, GB/s of logits
+read and ids/weights written, fraction of measured HBM).
 
 Timing: the call is captured once in a CUDA graph; every timed step flushes
 L2 (a 256 MiB write, outside the timed events) and replays the graph between
@@ -341,6 +344,30 @@ def main():
                                   "hbm_frac": round(wms["call_bytes"] / us / 1e3 / hbm, 3)}
                 del gs
 
+        # ---- gating kernel (router logits -> topk ids / weights), bench M and
+        # M=16384: event timing of one launch, L2 flushed before each
+        router = {}
+        if not args.no_sweep:
+            for Mr in (M, 16384):
+                gr = torch.Generator().manual_seed(5000 + Mr)
+                logits = torch.randn(Mr, shape.E, generator=gr, dtype=torch.float32).to(dev)
+                for _ in range(3):
+                    m.moe_router_topk(logits, k, stream=stream)
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(20):
+                    flush.zero_()
+                    e_s.record(stream)
+                    m.moe_router_topk(logits, k, stream=stream)
+                    e_e.record(stream)
+                    e_e.synchronize()
+                    ts.append(e_s.elapsed_time(e_e))
+                us = statistics.median(ts) * 1000
+                nbytes = Mr * shape.E * 4 + Mr * k * 8
+                router[str(Mr)] = {"us": round(us, 2), "bytes": nbytes,
+                                   "gbs": round(nbytes / us / 1e3, 1),
+                                   "hbm_frac": round(nbytes / us / 1e3 / hbm, 3)}
+
     # ---- roofline of the dominant kernel
     dom = max(("stage1_gemm", "stage2_gemm"), key=lambda kk: kmean[kk])
     dom_bytes = wm["stage1_bytes"] if dom == "stage1_gemm" else wm["stage2_bytes"]
@@ -371,6 +398,8 @@ def main():
     }
     if sweep:
         line["sweep"] = sweep
+    if router:
+        line["router"] = router
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, shape)
     if rank == 0:

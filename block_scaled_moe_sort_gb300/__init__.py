@@ -18,7 +18,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "lib", "MoeError", "moe_sort", "moe_sort_max_padded", "moe_quant_act_mx",
+    "lib", "MoeError", "moe_sort", "moe_sort_max_padded", "moe_quant_act_mx", "moe_router_topk",
     "moe_prepack_scales_mx", "moe_prepack_weights_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
     "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS", "fused_moe_a8w4_noalloc",
@@ -52,6 +52,8 @@ _SIGS = {
                           _c_size_t, _c_void_p]),
     "moe_quant_act_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_void_p,
                                   _c_void_p]),
+    "moe_router_topk": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p,
+                                 _c_void_p, _c_void_p]),
     "moe_prepacked_scale_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
     "moe_prepacked_weight_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
     "moe_prepack_weights_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p,
@@ -165,6 +167,23 @@ def moe_sort(topk_ids: torch.Tensor, topk_weights: torch.Tensor, E: int, block_m
                           _ptr(out["route_pos"]), _ptr(ws), nws, _stream(stream))
     _check("moe_sort", code)
     return out
+
+
+# ---------------------------------------------------------------- gating
+
+def moe_router_topk(logits: torch.Tensor, topk: int, shared_id: Optional[int] = None,
+                    stream=None):
+    """Router logits float32 [M, E] -> (topk_ids int32 [M, k'], topk_weights
+    float32 [M, k']), k' = topk (+1 with a shared expert of weight 1)."""
+    assert logits.dtype == torch.float32 and logits.dim() == 2 and logits.stride(1) == 1
+    M, E = logits.shape
+    kout = topk + (1 if shared_id is not None else 0)
+    ids = torch.empty(M, kout, dtype=torch.int32, device=logits.device)
+    w = torch.empty(M, kout, dtype=torch.float32, device=logits.device)
+    _check("moe_router_topk", lib().moe_router_topk(
+        _ptr(logits), M, E, logits.stride(0), topk, -1 if shared_id is None else shared_id,
+        _ptr(ids), _ptr(w), _stream(stream)))
+    return ids, w
 
 
 # ---------------------------------------------------------------- quant

@@ -279,6 +279,17 @@ moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_router_topk(const float* logits, int M, int E, int ld, int topk, int shared_id,
+                             int32_t* topk_ids, float* topk_weights, moe_stream_t stream) {
+  if (M < 0 || E <= 0 || ld < E || topk < 1 || topk > E) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || topk + (shared_id >= 0 ? 1 : 0) > kMaxTopk) return MOE_ERR_UNSUPPORTED;
+  if (M > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!aligned(logits) || !aligned(topk_ids) || !aligned(topk_weights)))
+    return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_router_topk(logits, M, E, ld, topk, shared_id, topk_ids, topk_weights,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_prepacked_weight_bytes(int E, int N, int K) {
   if (E <= 0 || N <= 0 || K <= 0 || N % 128 || K % 128) return 0;
   return static_cast<size_t>(E) * N * (K / 2);

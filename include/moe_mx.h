@@ -96,6 +96,28 @@ moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M,
                       int32_t* block_expert, int32_t* expert_off, int32_t* num_padded,
                       int32_t* route_pos, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ------------------------------------------------------------------ gating
+ * moe_router_topk: router logits -> topk_ids / topk_weights for moe_sort and
+ * the fused calls (the gating the pages time together with the layer, AITER
+ * #5609 "Add DeepSeek V4.1 Flash TP4 gfx950 MoE tuning", Performance on the
+ * measured runtime). Per token t:
+ *   - the topk experts with the largest logits[t, e]; equal logits are taken
+ *     in ascending expert order; columns are in that order (descending
+ *     logit, then ascending expert);
+ *   - weight of a pick = softmax of the picks' logits (FP32 arithmetic);
+ *   - if shared_id >= 0, one more column holds shared_id with weight 1.0
+ *     (the 385-expert top-7 layout: the shared expert is id E).
+ * logits: float32 [M, E], row stride ld >= E elements, finite values.
+ * topk_ids int32 / topk_weights float32: [M, topk (+1 with a shared expert)],
+ *   caller-allocated device memory, fully written.
+ * Errors (before any launch): MOE_ERR_INVALID_ARG for M < 0, E < 1, ld < E,
+ * topk outside [1, E] or a NULL pointer with M > 0; MOE_ERR_UNSUPPORTED for
+ * E > 512 or more than 16 output columns; MOE_ERR_ALIGNMENT for pointers not
+ * 256-byte aligned. M == 0 launches nothing.
+ */
+moe_status_t moe_router_topk(const float* logits, int M, int E, int ld, int topk, int shared_id,
+                             int32_t* topk_ids, float* topk_weights, moe_stream_t stream);
+
 /* -------------------------------------------------------- activation quant
  * moe_quant_act_mx: x BF16 [M, K] (row stride ldx elements) -> q E4M3 codes
  * [M, K] (row stride K) and scale E8M0 bytes [M, K/32]. Per 1x32 block:

@@ -16,7 +16,7 @@ def L():
 
 def test_header_declares_the_entry_points():
     names = m.declared_functions()
-    for want in ["moe_sort", "moe_quant_act_mx", "fused_moe_a8w4", "fused_moe_a16w4",
+    for want in ["moe_sort", "moe_quant_act_mx", "fused_moe_a8w4", "fused_moe_a16w4", "moe_router_topk",
                  "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "moe_status_string"]:
         assert want in names
 
@@ -100,3 +100,16 @@ def test_sort_and_quant_reject_bad_arguments(L):
 def test_device_status_decoding(L):
     assert L.moe_decode_device_status(0) == 0
     assert L.moe_decode_device_status(1) == 6
+
+
+def test_router_rejects_bad_arguments_on_host(L):
+    def call(M=4, E=384, ld=384, k=6, shared=-1, lg=FAKE, ids=FAKE, w=FAKE):
+        return L.moe_router_topk(lg, M, E, ld, k, shared, ids, w, None)
+    assert call(M=-1) == 1
+    assert call(ld=100) == 1                   # ld < E
+    assert call(k=0) == 1 and call(E=4, ld=4, k=5) == 1
+    assert call(lg=None) == 1
+    assert call(E=600, ld=600) == 2            # > 512 experts
+    assert call(k=16, shared=384) == 2         # 17 output columns
+    assert call(w=FAKE + 4) == 4               # misaligned
+    assert call(M=0, lg=None, ids=None, w=None) == 0   # empty call, no launch
