@@ -67,6 +67,14 @@ _SIGS = {
     "fused_moe_a16w4": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                  _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
                                  _c_void_p, _c_void_p, _c_size_t, _c_void_p]),
+    "fused_moe_workspace_bytes_bm": (_c_size_t, [_c_int] * 7),
+    "fused_moe_workspace_layout_bm": (_c_int, [_c_int] * 7 + [ctypes.POINTER(MoeWsLayout)]),
+    "fused_moe_a8w4_bm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                   _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
+                                   _c_void_p, _c_void_p, _c_size_t, _c_int, _c_void_p]),
+    "fused_moe_a16w4_bm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                    _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
+                                    _c_void_p, _c_void_p, _c_size_t, _c_int, _c_void_p]),
     "moe_decode_device_status": (_c_int, [ctypes.c_int32]),
     "fused_moe_a8w4_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
@@ -229,19 +237,30 @@ def moe_prepack_scales_mx(scale: torch.Tensor, stream=None) -> torch.Tensor:
 
 # ---------------------------------------------------------- fused layer
 
-def fused_moe_workspace_bytes(M: int, H: int, Ip: int, E: int, topk: int, a16: bool) -> int:
+def fused_moe_workspace_bytes(M: int, H: int, Ip: int, E: int, topk: int, a16: bool,
+                              block_m: int = 0) -> int:
+    """Workspace size; block_m 0 = the library's rule, else the route block
+    asked for (fused_moe_workspace_bytes_bm)."""
+    if block_m:
+        return int(lib().fused_moe_workspace_bytes_bm(M, H, Ip, E, topk, int(a16), block_m))
     return int(lib().fused_moe_workspace_bytes(M, H, Ip, E, topk, int(a16)))
 
 
-def fused_moe_workspace_layout(M: int, H: int, Ip: int, E: int, topk: int, a16: bool) -> dict:
+def fused_moe_workspace_layout(M: int, H: int, Ip: int, E: int, topk: int, a16: bool,
+                               block_m: int = 0) -> dict:
     L = MoeWsLayout()
-    _check("fused_moe_workspace_layout",
-           lib().fused_moe_workspace_layout(M, H, Ip, E, topk, int(a16), ctypes.byref(L)))
+    if block_m:
+        _check("fused_moe_workspace_layout_bm",
+               lib().fused_moe_workspace_layout_bm(M, H, Ip, E, topk, int(a16), block_m,
+                                                   ctypes.byref(L)))
+    else:
+        _check("fused_moe_workspace_layout",
+               lib().fused_moe_workspace_layout(M, H, Ip, E, topk, int(a16), ctypes.byref(L)))
     return {f: getattr(L, f) for f, _ in MoeWsLayout._fields_ if f != "_pad"}
 
 
 def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
-           E, Ip, out=None, ws=None, stream=None):
+           E, Ip, out=None, ws=None, stream=None, block_m=0):
     M, H = x.shape
     topk = topk_ids.shape[1]
     a16 = fn_name == "fused_moe_a16w4"
@@ -251,30 +270,35 @@ def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
     if out is None:
         out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
     if ws is None:
-        ws = torch.empty(max(fused_moe_workspace_bytes(M, H, Ip, E, topk, a16), 1),
+        ws = torch.empty(max(fused_moe_workspace_bytes(M, H, Ip, E, topk, a16, block_m), 1),
                          dtype=torch.uint8, device=x.device)
-    code = getattr(lib(), fn_name)(
-        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, H, topk, _ptr(w1),
-        _ptr(w1_scale_packed), _ptr(w2), _ptr(w2_scale_packed), E, Ip, _ptr(out), _ptr(ws),
-        ws.numel(), _stream(stream))
+    args = [_ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, H, topk, _ptr(w1),
+            _ptr(w1_scale_packed), _ptr(w2), _ptr(w2_scale_packed), E, Ip, _ptr(out), _ptr(ws),
+            ws.numel()]
+    if block_m:
+        fn_name = fn_name + "_bm"
+        args.append(block_m)
+    code = getattr(lib(), fn_name)(*args, _stream(stream))
     _check(fn_name, code)
     return out
 
 
 def fused_moe_a8w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
-                   w2_scale_packed, E, Ip, out=None, ws=None, stream=None) -> torch.Tensor:
+                   w2_scale_packed, E, Ip, out=None, ws=None, stream=None,
+                   block_m: int = 0) -> torch.Tensor:
     """FP8-activation x MXFP4-weight fused MoE on prepacked weights; returns
-    BF16 [M, H]."""
+    BF16 [M, H]. block_m 0 = the library's route block rule."""
     return _fused("fused_moe_a8w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
-                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream)
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m)
 
 
 def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
-                    w2_scale_packed, E, Ip, out=None, ws=None, stream=None) -> torch.Tensor:
+                    w2_scale_packed, E, Ip, out=None, ws=None, stream=None,
+                    block_m: int = 0) -> torch.Tensor:
     """BF16-activation x MXFP4-weight fused MoE on prepacked weights; returns
-    BF16 [M, H]."""
+    BF16 [M, H]. block_m 0 = the library's route block rule."""
     return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
-                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream)
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m)
 
 
 NOALLOC_WORKSPACE_BYTES = 16 << 20
@@ -312,22 +336,60 @@ def moe_profile_collect() -> tuple:
 
 
 class MoeLayer:
-    """Device-resident MXFP4 expert weights with prepacked scales."""
+    """Device-resident MXFP4 expert weights with prepacked scales.
 
-    def __init__(self, w1, w1_scale, w2, w2_scale, a16: bool = False, device="cuda"):
+    block_m_table: rows (max_tokens, block_m) sorted by max_tokens (see
+    block_scaled_moe_sort_gb300.tune): a call with M tokens uses the route
+    block of the first row with M <= max_tokens; beyond the last row, or
+    without a table, the library's own rule applies. "gb300" takes the rows
+    of this geometry from the table shipped with the package."""
+
+    def __init__(self, w1, w1_scale, w2, w2_scale, a16: bool = False, device="cuda",
+                 block_m_table=None):
         self.a16 = a16
         self.E = w1.shape[0]
         self.H = w2.shape[1]
         self.Ip = w2.shape[2] * 2
+        self._bm_by_topk = None          # shipped rows of this geometry, per topk
+        if isinstance(block_m_table, str):
+            if block_m_table != "gb300":
+                raise ValueError("block_m_table: rows, None or 'gb300'")
+            from . import tune
+            self._bm_by_topk = {}
+            for r in tune.read_table(tune.PACKAGED_TABLE):
+                if (r["H"], r["Ip"], r["E"], r["a16"]) == (self.H, self.Ip, self.E, int(a16)):
+                    self._bm_by_topk.setdefault(r["topk"], []).append(
+                        (r["max_tokens"], r["block_m"]))
+            for rows in self._bm_by_topk.values():
+                rows.sort()
+            block_m_table = None
+        self.block_m_table = sorted(block_m_table) if block_m_table else []
         self.w1 = moe_prepack_weights_mx(w1.to(device).contiguous())
         self.w2 = moe_prepack_weights_mx(w2.to(device).contiguous())
         self.w1_scale = moe_prepack_scales_mx(w1_scale.to(device).contiguous())
         self.w2_scale = moe_prepack_scales_mx(w2_scale.to(device).contiguous())
 
-    def workspace_bytes(self, M: int, topk: int) -> int:
-        return fused_moe_workspace_bytes(M, self.H, self.Ip, self.E, topk, self.a16)
+    def block_m_for(self, M: int, topk: Optional[int] = None) -> int:
+        """Route block for an M-token call (0 = the library's rule)."""
+        table = self.block_m_table
+        by_topk = getattr(self, "_bm_by_topk", None)
+        if by_topk is not None:
+            table = by_topk.get(topk, [])
+        for max_tokens, bm in table:
+            if M <= max_tokens:
+                return int(bm)
+        return 0
 
-    def __call__(self, x, topk_ids, topk_weights, out=None, ws=None, stream=None):
+    def workspace_bytes(self, M: int, topk: int) -> int:
+        return fused_moe_workspace_bytes(M, self.H, self.Ip, self.E, topk, self.a16,
+                                         self.block_m_for(M, topk))
+
+    def workspace_layout(self, M: int, topk: int) -> dict:
+        return fused_moe_workspace_layout(M, self.H, self.Ip, self.E, topk, self.a16,
+                                          self.block_m_for(M, topk))
+
+    def __call__(self, x, topk_ids, topk_weights, out=None, ws=None, stream=None, block_m=None):
         fn = fused_moe_a16w4 if self.a16 else fused_moe_a8w4
+        bm = self.block_m_for(x.shape[0], topk_ids.shape[1]) if block_m is None else block_m
         return fn(x, topk_ids, topk_weights, self.w1, self.w1_scale, self.w2, self.w2_scale,
-                  self.E, self.Ip, out=out, ws=ws, stream=stream)
+                  self.E, self.Ip, out=out, ws=ws, stream=stream, block_m=bm)

@@ -64,9 +64,11 @@ moe_status_t check_shape(int M, int H, int Ip, int E, int topk) {
   return MOE_OK;
 }
 
-void build_layout(int M, int H, int Ip, int E, int topk, bool a16, moe_ws_layout_t* L) {
+// bm_req: the route block asked for (0 = choose_block_m)
+void build_layout(int M, int H, int Ip, int E, int topk, bool a16, int bm_req,
+                  moe_ws_layout_t* L) {
   std::memset(L, 0, sizeof(*L));
-  const int bm = choose_block_m(M, topk, E);
+  const int bm = bm_req > 0 ? bm_req : choose_block_m(M, topk, E);
   const int64_t R = static_cast<int64_t>(M) * topk;
   const int64_t pm = max_padded(R, E, bm);
   const int64_t nblk = pm / bm;
@@ -131,16 +133,17 @@ void prof_end_call() {
 moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const float* wts, int M,
                             int H, int topk, const uint8_t* w1, const uint8_t* w1s,
                             const uint8_t* w2, const uint8_t* w2s, int E, int Ip, void* out,
-                            void* ws, size_t ws_bytes, cudaStream_t s) {
+                            void* ws, size_t ws_bytes, int bm_req, cudaStream_t s) {
   moe_status_t st = check_shape(M, H, Ip, E, topk);
   if (st != MOE_OK) return st;
+  if (bm_req != 0 && !valid_bm(bm_req)) return MOE_ERR_UNSUPPORTED;
   if (!ws || !w1 || !w1s || !w2 || !w2s) return MOE_ERR_INVALID_ARG;
   if (M > 0 && (!x || !ids || !wts || !out)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, ids, wts, w1, w1s, w2, w2s, out, ws};
   for (const void* p : ptrs)
     if (p && !aligned(p)) return MOE_ERR_ALIGNMENT;
   moe_ws_layout_t L;
-  build_layout(M, H, Ip, E, topk, a16, &L);
+  build_layout(M, H, Ip, E, topk, a16, bm_req, &L);
   if (ws_bytes < static_cast<size_t>(L.total_bytes)) return MOE_ERR_WORKSPACE;
   if (M == 0) return MOE_OK;
 
@@ -318,36 +321,65 @@ moe_status_t moe_prepack_scales_mx(const uint8_t* scale, int E, int N, int K, ui
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t fused_moe_workspace_bytes(int M, int H, int Ip, int E, int topk, int a16) {
+size_t fused_moe_workspace_bytes_bm(int M, int H, int Ip, int E, int topk, int a16, int block_m) {
   if (check_shape(M, H, Ip, E, topk) != MOE_OK) return 0;
+  if (block_m != 0 && !valid_bm(block_m)) return 0;
   moe_ws_layout_t L;
-  build_layout(M, H, Ip, E, topk, a16 != 0, &L);
+  build_layout(M, H, Ip, E, topk, a16 != 0, block_m, &L);
   return static_cast<size_t>(L.total_bytes);
+}
+
+size_t fused_moe_workspace_bytes(int M, int H, int Ip, int E, int topk, int a16) {
+  return fused_moe_workspace_bytes_bm(M, H, Ip, E, topk, a16, 0);
+}
+
+moe_status_t fused_moe_workspace_layout_bm(int M, int H, int Ip, int E, int topk, int a16,
+                                           int block_m, moe_ws_layout_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_shape(M, H, Ip, E, topk);
+  if (st != MOE_OK) return st;
+  if (block_m != 0 && !valid_bm(block_m)) return MOE_ERR_UNSUPPORTED;
+  build_layout(M, H, Ip, E, topk, a16 != 0, block_m, out);
+  return MOE_OK;
 }
 
 moe_status_t fused_moe_workspace_layout(int M, int H, int Ip, int E, int topk, int a16,
                                         moe_ws_layout_t* out) {
-  if (!out) return MOE_ERR_INVALID_ARG;
-  moe_status_t st = check_shape(M, H, Ip, E, topk);
-  if (st != MOE_OK) return st;
-  build_layout(M, H, Ip, E, topk, a16 != 0, out);
-  return MOE_OK;
+  return fused_moe_workspace_layout_bm(M, H, Ip, E, topk, a16, 0, out);
+}
+
+moe_status_t fused_moe_a8w4_bm(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                               int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                               const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                               void* out, void* ws, size_t ws_bytes, int block_m,
+                               moe_stream_t stream) {
+  return fused_moe_impl(false, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
+                        E, Ip, out, ws, ws_bytes, block_m, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                                int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                                const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                                void* out, void* ws, size_t ws_bytes, int block_m,
+                                moe_stream_t stream) {
+  return fused_moe_impl(true, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
+                        E, Ip, out, ws, ws_bytes, block_m, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t fused_moe_a8w4(const void* x, const int32_t* topk_ids, const float* topk_weights,
                             int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
                             const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip, void* out,
                             void* ws, size_t ws_bytes, moe_stream_t stream) {
-  return fused_moe_impl(false, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
-                        E, Ip, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return fused_moe_a8w4_bm(x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale, E,
+                           Ip, out, ws, ws_bytes, 0, stream);
 }
 
 moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids, const float* topk_weights,
                              int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
                              const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip, void* out,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
-  return fused_moe_impl(true, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
-                        E, Ip, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return fused_moe_a16w4_bm(x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale, E,
+                            Ip, out, ws, ws_bytes, 0, stream);
 }
 
 moe_status_t moe_profile_enable(int enable) {

@@ -216,6 +216,29 @@ moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids,
                              const uint8_t* w2_scale, int E, int Ip, void* out, void* ws,
                              size_t ws_bytes, moe_stream_t stream);
 
+/* ------------------------------------------- explicit route block (tuning)
+ * The same calls with the route block chosen by the caller instead of the
+ * library's rule (the sort block = the GEMMs' route tile, the knob a
+ * per-token-bucket tuning table sets; AITER #5609 "Add DeepSeek V4.1 Flash
+ * TP4 gfx950 MoE tuning", Commands run: the sort block must equal the GEMM
+ * block). block_m: 0 for the library's rule, else one of 16, 32, 64, 128,
+ * 256; any other value gives 0 bytes / MOE_ERR_UNSUPPORTED. A workspace and
+ * its layout are valid only for the block_m they were sized with. The
+ * result is the same for every block_m up to FP32 summation order. */
+size_t fused_moe_workspace_bytes_bm(int M, int H, int Ip, int E, int topk, int a16, int block_m);
+moe_status_t fused_moe_workspace_layout_bm(int M, int H, int Ip, int E, int topk, int a16,
+                                           int block_m, moe_ws_layout_t* out /* host */);
+moe_status_t fused_moe_a8w4_bm(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                               int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                               const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                               void* out, void* ws, size_t ws_bytes, int block_m,
+                               moe_stream_t stream);
+moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                                int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                                const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                                void* out, void* ws, size_t ws_bytes, int block_m,
+                                moe_stream_t stream);
+
 /* ------------------------------------------------ no-allocation variant
  * fused_moe_a8w4_noalloc: fused_moe_a8w4 without a caller workspace. The
  * pages have no counterpart of this entry point; it exists for callers that

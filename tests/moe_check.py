@@ -82,7 +82,7 @@ def compare(case: mi.MoeCase, layer: m.MoeLayer, a16: bool, tokens=None, check_i
     out, ws = run_case(layer, case)
     M, k = case.M, case.topk_ids.shape[1]
     E, H, Ip = layer.E, layer.H, layer.Ip
-    lay = m.fused_moe_workspace_layout(M, H, Ip, E, k, a16)
+    lay = layer.workspace_layout(M, k)
     bm, pm = lay["block_m"], lay["p_max"]
     ref = om.fused_moe(case.x, case.topk_ids, case.topk_weights, case.w1, case.w1_scale,
                        case.w2, case.w2_scale, E, a16=a16, block_m=bm, tokens=tokens)

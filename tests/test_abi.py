@@ -113,3 +113,16 @@ def test_router_rejects_bad_arguments_on_host(L):
     assert call(k=16, shared=384) == 2         # 17 output columns
     assert call(w=FAKE + 4) == 4               # misaligned
     assert call(M=0, lg=None, ids=None, w=None) == 0   # empty call, no launch
+
+
+def test_explicit_block_m_validation(L):
+    assert L.fused_moe_workspace_bytes_bm(96, 5120, 640, 384, 6, 0, 48) == 0
+    for bm in (16, 32, 64, 128, 256):
+        n = L.fused_moe_workspace_bytes_bm(96, 5120, 640, 384, 6, 0, bm)
+        lay = m.fused_moe_workspace_layout(96, 5120, 640, 384, 6, False, bm)
+        assert n == lay["total_bytes"] > 0 and lay["block_m"] == bm
+    assert (L.fused_moe_workspace_bytes_bm(96, 5120, 640, 384, 6, 1, 0)
+            == L.fused_moe_workspace_bytes(96, 5120, 640, 384, 6, 1))
+    args = [FAKE, FAKE, FAKE, 4, 256, 2, FAKE, FAKE, FAKE, FAKE, 8, 128, FAKE, FAKE, 1 << 40]
+    assert L.fused_moe_a8w4_bm(*args, 24, None) == 2
+    assert L.fused_moe_a16w4_bm(*args, 512, None) == 2

@@ -35,6 +35,20 @@ def test_small_geometry_full(cuda_lib, a16, M):
     print(st)
 
 
+@pytest.mark.parametrize("a16", [False, True])
+@pytest.mark.parametrize("bm", [16, 32, 64, 128, 256])
+def test_explicit_block_m(cuda_lib, a16, bm):
+    # the route block a tuning table sets (the *_bm entry points): every
+    # supported block on both variants, several tiles and a ragged tail
+    shp = mi.small_shape(H=512, I=192, Ip=256, E=8, topk=3, E_route=10, a16=a16)
+    w = mi.make_weights(shp, 5)
+    layer = m.MoeLayer(w["w1"], w["w1_scale"], w["w2"], w["w2_scale"], a16=a16,
+                       block_m_table=[(1 << 30, bm)])
+    case = mi.make_case("small", 130, shape=shp, weights=w)
+    st = compare(case, layer, a16)
+    assert st["block_m"] == bm
+
+
 def test_empty_experts_and_all_dropped_tokens(cuda_lib):
     shp = mi.small_shape(H=256, I=128, Ip=128, E=16, topk=2, E_route=64)
     w, layer = _small_layer(shp, 9)
