@@ -335,6 +335,19 @@ def moe_profile_collect() -> tuple:
     return dict(zip(PROFILE_SLOTS, list(ms))), int(n.value)
 
 
+def shipped_block_m_rows(H: int, Ip: int, E: int, a16: bool) -> dict:
+    """The shipped GB300 tuning rows of one geometry: topk -> sorted
+    [(max_tokens, block_m), ...] (empty for a geometry that was not tuned)."""
+    from . import tune
+    by_topk = {}
+    for r in tune.read_table(tune.PACKAGED_TABLE):
+        if (r["H"], r["Ip"], r["E"], r["a16"]) == (H, Ip, E, int(a16)):
+            by_topk.setdefault(r["topk"], []).append((r["max_tokens"], r["block_m"]))
+    for rows in by_topk.values():
+        rows.sort()
+    return by_topk
+
+
 class MoeLayer:
     """Device-resident MXFP4 expert weights with prepacked scales.
 
@@ -354,14 +367,7 @@ class MoeLayer:
         if isinstance(block_m_table, str):
             if block_m_table != "gb300":
                 raise ValueError("block_m_table: rows, None or 'gb300'")
-            from . import tune
-            self._bm_by_topk = {}
-            for r in tune.read_table(tune.PACKAGED_TABLE):
-                if (r["H"], r["Ip"], r["E"], r["a16"]) == (self.H, self.Ip, self.E, int(a16)):
-                    self._bm_by_topk.setdefault(r["topk"], []).append(
-                        (r["max_tokens"], r["block_m"]))
-            for rows in self._bm_by_topk.values():
-                rows.sort()
+            self._bm_by_topk = shipped_block_m_rows(self.H, self.Ip, self.E, a16)
             block_m_table = None
         self.block_m_table = sorted(block_m_table) if block_m_table else []
         self.w1 = moe_prepack_weights_mx(w1.to(device).contiguous())

@@ -104,3 +104,14 @@ def test_layer_lookup_by_topk_for_shipped_rows():
                                 _bm_by_topk={3: [(512, 16), (1024, 32)], 6: [(1024, 16)]})
     f = MoeLayer.block_m_for
     assert f(lay, 640, 3) == 32 and f(lay, 640, 6) == 16 and f(lay, 640, 4) == 0
+
+
+def test_shipped_rows_by_geometry():
+    from block_scaled_moe_sort_gb300 import shipped_block_m_rows
+    draft = shipped_block_m_rows(5120, 640, 128, False)
+    assert list(draft) == [3] and draft[3][-1] == (1024, 32)
+    backbone = shipped_block_m_rows(5120, 640, 384, False)
+    assert [bm for _, bm in backbone[6]] == [16] * 8
+    assert shipped_block_m_rows(5120, 2304, 96, False) == {}     # not tuned
+    lay = types.SimpleNamespace(block_m_table=[], _bm_by_topk=draft)
+    assert MoeLayer.block_m_for(lay, 640, 3) == 32 and MoeLayer.block_m_for(lay, 320, 3) == 16
