@@ -85,6 +85,20 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value; every rank gets it (the job's time
+    is its slowest rank's)."""
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def us_per_call(total_ms: float, steps: int, world: int) -> float:
+    """Whole-job µs per call: each of `world` replicas ran `steps` calls
+    within the slowest rank's total_ms."""
+    return total_ms * 1000 / (steps * world)
+
+
 def work_model(shape, ids, M):
     """Algorithmic bytes and flops of one call (valid routes, touched experts)."""
     E, H, Ip, k = shape.E, shape.H, shape.Ip, ids.shape[1]
@@ -282,10 +296,8 @@ def main():
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         total_ms = sum(step_ms)
         if world > 1:
-            t = torch.tensor([total_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            total_ms = float(t.item())
-        us_per_call = total_ms * 1000 / (args.steps * world)
+            total_ms = max_over_ranks(total_ms, dev)
+        call_us = us_per_call(total_ms, args.steps, world)
 
         # ---- per-kernel timing pass (eager calls, events around each kernel)
         m.moe_profile_enable(True)
@@ -380,13 +392,13 @@ def main():
             "algorithmic_bytes": int(dom_bytes), "kernel_us": round(dom_ms * 1000, 2)}
 
     line = {
-        "metric": METRIC, "value": round(us_per_call, 2), "unit": "us/call", "n_gpus": world,
+        "metric": METRIC, "value": round(call_us, 2), "unit": "us/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 x mxfp4 (fp32 accumulate)",
         "data": "synthetic (seeded, random-init weights)", "config": config_dict(M, world),
-        "tflops": round(wm["flops"] / us_per_call / 1e6, 2),
-        "call_hbm_frac": round(wm["call_bytes"] / us_per_call / 1e3 / hbm, 4),
+        "tflops": round(wm["flops"] / call_us / 1e6, 2),
+        "call_hbm_frac": round(wm["call_bytes"] / call_us / 1e3 / hbm, 4),
         "kernels_us": {kk: round(v * 1000, 2) for kk, v in kmean.items()},
         "roofline": roof,
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call",
