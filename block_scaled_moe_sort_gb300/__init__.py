@@ -76,6 +76,7 @@ _SIGS = {
                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
                                     _c_void_p, _c_void_p, _c_size_t, _c_int, _c_void_p]),
     "moe_decode_device_status": (_c_int, [ctypes.c_int32]),
+    "moe_debug_wait_selftest": (_c_int, [_c_void_p, _c_int, _c_void_p]),
     "fused_moe_a8w4_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
                                         _c_int, _c_void_p, _c_void_p]),
@@ -175,6 +176,20 @@ def moe_sort(topk_ids: torch.Tensor, topk_weights: torch.Tensor, E: int, block_m
                           _ptr(out["route_pos"]), _ptr(ws), nws, _stream(stream))
     _check("moe_sort", code)
     return out
+
+
+# ------------------------------------------------------ failure reporting
+
+def moe_debug_wait_selftest(timeout_us: int = 1000, device="cuda", stream=None):
+    """Run the bounded-wait self-test (a wait on a barrier nothing completes)
+    and return (decoded status, returned marker): (MOE_ERR_TIMEOUT = 6, 1)
+    when the wait gave up and the kernel returned. Synchronises."""
+    st = torch.zeros(2, dtype=torch.int32, device=device)
+    _check("moe_debug_wait_selftest",
+           lib().moe_debug_wait_selftest(_ptr(st), timeout_us, _stream(stream)))
+    torch.cuda.synchronize(st.device)
+    word, returned = st.cpu().tolist()
+    return int(lib().moe_decode_device_status(word)), int(returned)
 
 
 # ---------------------------------------------------------------- gating

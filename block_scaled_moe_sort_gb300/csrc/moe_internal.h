@@ -20,6 +20,8 @@ cudaError_t launch_sort(const int32_t* ids, const float* wts, int R, int E, int 
 cudaError_t launch_quant_act(const void* x, int M, int K, int ldx, uint8_t* q, uint8_t* scale,
                              cudaStream_t s);
 
+cudaError_t launch_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
+
 cudaError_t launch_router_topk(const float* logits, int M, int E, int ld, int topk,
                                int shared_id, int32_t* ids, float* weights, cudaStream_t s);
 

@@ -404,6 +404,13 @@ moe_status_t moe_profile_collect(double* kernel_ms, int32_t* n_calls) {
   return MOE_OK;
 }
 
+moe_status_t moe_debug_wait_selftest(int32_t* status, int timeout_us, moe_stream_t stream) {
+  if (!status || timeout_us < 1 || timeout_us > 1000000) return MOE_ERR_INVALID_ARG;
+  if (!aligned(status)) return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_wait_selftest(status, static_cast<uint64_t>(timeout_us) * 1000u,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_decode_device_status(int32_t status_word) {
   return (status_word & kDevTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
 }

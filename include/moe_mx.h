@@ -289,6 +289,16 @@ moe_status_t moe_profile_collect(double* kernel_ms, int32_t* n_calls);
  * moe_status_t: MOE_OK, or MOE_ERR_TIMEOUT if a device wait gave up. */
 moe_status_t moe_decode_device_status(int32_t status_word);
 
+/* Self-test of the device-side failure reporting: one kernel waits, with the
+ * same bounded wait every kernel of the layer uses, on a barrier that
+ * nothing completes; after timeout_us (1 .. 1e6) of global time the wait
+ * gives up, ORs the timeout bit into status[0] and the kernel writes
+ * status[1] = 1 and returns (2 would mean the wait completed). status: device
+ * int32[2], zeroed by the caller, 256-byte aligned. The GPU is neither hung
+ * nor faulted and the context stays usable. MOE_ERR_INVALID_ARG /
+ * MOE_ERR_ALIGNMENT before any launch. */
+moe_status_t moe_debug_wait_selftest(int32_t* status, int timeout_us, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

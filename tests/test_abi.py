@@ -126,3 +126,10 @@ def test_explicit_block_m_validation(L):
     args = [FAKE, FAKE, FAKE, 4, 256, 2, FAKE, FAKE, FAKE, FAKE, 8, 128, FAKE, FAKE, 1 << 40]
     assert L.fused_moe_a8w4_bm(*args, 24, None) == 2
     assert L.fused_moe_a16w4_bm(*args, 512, None) == 2
+
+
+def test_wait_selftest_rejects_bad_arguments_on_host(L):
+    assert L.moe_debug_wait_selftest(None, 1000, None) == 1
+    assert L.moe_debug_wait_selftest(FAKE, 0, None) == 1
+    assert L.moe_debug_wait_selftest(FAKE, 2000000, None) == 1
+    assert L.moe_debug_wait_selftest(FAKE + 4, 1000, None) == 4
