@@ -350,6 +350,21 @@ def moe_profile_collect() -> tuple:
     return dict(zip(PROFILE_SLOTS, list(ms))), int(n.value)
 
 
+def with_shared_expert(w1, w1_scale, w2, w2_scale, shared):
+    """Routed expert tensors [E, ...] plus one separate shared expert's
+    (w1 [2*Ip, H/2] or [1, 2*Ip, H/2], its scales, w2, its scales) -> the
+    same tensors with the shared expert appended as expert E (load-time data
+    preparation before the one-time prepack)."""
+    out = []
+    for routed, sh in zip((w1, w1_scale, w2, w2_scale), shared):
+        sh = sh if sh.dim() == routed.dim() else sh.unsqueeze(0)
+        if sh.shape[0] != 1 or sh.shape[1:] != routed.shape[1:]:
+            raise ValueError(f"shared expert tensor of shape {tuple(sh.shape)} does not match "
+                             f"routed experts {tuple(routed.shape)}")
+        out.append(torch.cat([routed, sh.to(routed.device, routed.dtype)], dim=0))
+    return tuple(out)
+
+
 def shipped_block_m_rows(H: int, Ip: int, E: int, a16: bool) -> dict:
     """The shipped GB300 tuning rows of one geometry: topk -> sorted
     [(max_tokens, block_m), ...] (empty for a geometry that was not tuned)."""
@@ -370,11 +385,24 @@ class MoeLayer:
     block_scaled_moe_sort_gb300.tune): a call with M tokens uses the route
     block of the first row with M <= max_tokens; beyond the last row, or
     without a table, the library's own rule applies. "gb300" takes the rows
-    of this geometry from the table shipped with the package."""
+    of this geometry from the table shipped with the package.
+
+    shared_expert: (w1, w1_scale, w2, w2_scale) of one separate shared
+    expert that every token uses with weight 1 (the shared-first layouts of
+    the pages: the 385-expert top-7 case). It is appended as expert E and
+    runs inside the same grouped GEMMs as the routed experts; ``route``
+    produces ids and weights with its column, which the call takes as they
+    are."""
 
     def __init__(self, w1, w1_scale, w2, w2_scale, a16: bool = False, device="cuda",
-                 block_m_table=None):
+                 block_m_table=None, shared_expert=None):
         self.a16 = a16
+        self.E_routed = w1.shape[0]
+        self.shared_id = None
+        if shared_expert is not None:
+            w1, w1_scale, w2, w2_scale = with_shared_expert(w1, w1_scale, w2, w2_scale,
+                                                            shared_expert)
+            self.shared_id = self.E_routed
         self.E = w1.shape[0]
         self.H = w2.shape[1]
         self.Ip = w2.shape[2] * 2
@@ -389,6 +417,12 @@ class MoeLayer:
         self.w2 = moe_prepack_weights_mx(w2.to(device).contiguous())
         self.w1_scale = moe_prepack_scales_mx(w1_scale.to(device).contiguous())
         self.w2_scale = moe_prepack_scales_mx(w2_scale.to(device).contiguous())
+
+    def route(self, logits: torch.Tensor, topk: int, stream=None):
+        """Router logits float32 [M, E_routed] -> (topk_ids, topk_weights) for
+        this layer, with the shared expert's column when it has one."""
+        assert logits.shape[1] == self.E_routed
+        return moe_router_topk(logits, topk, shared_id=self.shared_id, stream=stream)
 
     def block_m_for(self, M: int, topk: Optional[int] = None) -> int:
         """Route block for an M-token call (0 = the library's rule)."""

@@ -67,3 +67,25 @@ def test_router_feeds_the_fused_call(cuda_lib):
     case.topk_ids = ids.cpu()
     case.topk_weights = wt.cpu()
     print(compare(case, layer, False))
+
+
+@pytest.mark.parametrize("a16", [False, True])
+def test_separate_shared_expert(cuda_lib, a16):
+    # 8 routed experts plus one separate shared expert (weight 1 for every
+    # token), routed by the gating kernel; the oracle sees all 9 experts
+    shp = mi.small_shape(H=512, I=192, Ip=256, E=9, topk=4, E_route=8, a16=a16)
+    w = mi.make_weights(shp, 31)
+    routed = [w[k][:8] for k in ("w1", "w1_scale", "w2", "w2_scale")]
+    shared = [w[k][8] for k in ("w1", "w1_scale", "w2", "w2_scale")]
+    layer = m.MoeLayer(*routed, a16=a16, shared_expert=shared)
+    assert layer.E == 9 and layer.shared_id == 8
+    L = _logits(70, 8, 91)
+    ids, wt = layer.route(L.cuda(), 3)
+    ids_c, wt_c = ids.cpu(), wt.cpu()
+    assert (ids_c[:, 3] == 8).all() and (wt_c[:, 3] == 1.0).all()
+    ref_ids, _ = orr.router_topk(L.numpy(), 3, shared_id=8)
+    assert np.array_equal(ids_c.numpy(), ref_ids)
+    case = mi.make_case("small", 70, shape=shp, weights=w)
+    case.topk_ids = ids_c
+    case.topk_weights = wt_c
+    print(compare(case, layer, a16))
