@@ -111,8 +111,6 @@ class MoeResult:
     out_bf16: np.ndarray          # float64 [M or len(tokens), H], BF16 values
     out_f64: np.ndarray           # float64 pre-rounding sum
     sort: SortResult
-    xq: Optional[np.ndarray]      # uint8 [M, H] (a8w4) or None
-    xs: Optional[np.ndarray]      # uint8 [M, H/32]
     inter_rows: np.ndarray        # int64: sorted positions p of the rows below
     aq: np.ndarray                # uint8 [rows, Ip] FP8 codes (a8w4) / float64 BF16 values (a16w4)
     as_: Optional[np.ndarray]     # uint8 [rows, Ip/32] (a8w4)
@@ -150,14 +148,6 @@ def fused_moe(x, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, E: int,
 
     srt = moe_sort(ids, wts, E, block_m)
 
-    # step 2: activation quantisation (a8w4) - dequantised operand for step 3
-    if a16:
-        xq = xs = None
-        xdq = xf                                   # BF16 values are exact in FP64
-    else:
-        xq, xs = mx.quant_mxfp8(xf)
-        xdq = mx.dequant_mxfp8(xq, xs)
-
     tok_sel = np.arange(M) if tokens is None else np.asarray(tokens, dtype=np.int64)
     want_tok = np.zeros(M, dtype=bool)
     want_tok[tok_sel] = True
@@ -165,6 +155,19 @@ def fused_moe(x, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, E: int,
     if experts is not None:
         want_exp[:] = False
         want_exp[np.asarray(experts, dtype=np.int64)] = True
+
+    # step 2: activation quantisation (a8w4) - dequantised operand for step 3.
+    # The rule acts on each token row on its own, so only the rows of tokens
+    # that have a computed route are quantised.
+    if a16:
+        xdq = xf                                   # BF16 values are exact in FP64
+    else:
+        valid = (ids >= 0) & (ids < E)
+        used = want_tok & (valid & want_exp[np.where(valid, ids, 0)]).any(axis=1)
+        xdq = np.zeros_like(xf)
+        if used.any():
+            xq, xs = mx.quant_mxfp8(xf[used])
+            xdq[used] = mx.dequant_mxfp8(xq, xs)
 
     out = np.zeros((M, H), dtype=np.float64)
     inter_rows, aq_rows, as_rows = [], [], []
@@ -212,12 +215,5 @@ def fused_moe(x, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, E: int,
         rows = np.zeros(0, dtype=np.int64)
         aq_all = np.zeros((0, Ip), dtype=np.float64 if a16 else np.uint8)
         as_all = None if a16 else np.zeros((0, Ip // 32), dtype=np.uint8)
-    return MoeResult(mx.bf16_round(out_sel), out_sel, srt, xq, xs, rows, aq_all,
-                     as_all, tok_sel)
+    return MoeResult(mx.bf16_round(out_sel), out_sel, srt, rows, aq_all, as_all, tok_sel)
 
-
-def routes_per_expert(topk_ids, E: int) -> np.ndarray:
-    """Valid routes per expert (used to size work and for scaling)."""
-    ids = _np(topk_ids).astype(np.int64).reshape(-1)
-    ids = ids[(ids >= 0) & (ids < E)]
-    return np.bincount(ids, minlength=E)

@@ -105,11 +105,6 @@ def bf16_bits(v) -> np.ndarray:
     return (f32.view(np.uint32) >> 16).astype(np.uint16)
 
 
-def bf16_from_bits(bits) -> np.ndarray:
-    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
-    return b.view(np.float32).astype(np.float64)
-
-
 def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
     """uint8 [..., K/2] (element k in byte k/2, low nibble = even k) ->
     uint8 codes [..., K]."""
