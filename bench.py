@@ -11,6 +11,14 @@ and the gating kernel (router logits -> top-k ids and weights, 384 experts,
 top-6) at the bench M and at M=16384 under "router" (µs, GB/s of logits
 read and ids/weights written, fraction of measured HBM).
 
+The prefill half of the metric is reported under "prefill": the skewed
+prefill stress (backbone a8w4, M=16384, Zipf(1.2) routing) and the a16w4
+385-expert top-7 geometry with the fused shared expert at M=16384, each as
+µs/call, TFLOP/s, the fraction of the block-scaled MMA peak (a8w4: the FP8
+rate, taken as twice the measured BF16 GEMM rate; a16w4: the BF16 rate), the
+fraction of measured HBM bandwidth, and the fraction of the binding roofline
+max(bytes / HBM, flops / MMA peak) / time.
+
 Timing: the call is captured once in a CUDA graph; every timed step flushes
 L2 (a 256 MiB write, outside the timed events) and replays the graph between
 two CUDA events on the launching stream. W untimed warm-up steps come first;
@@ -41,12 +49,48 @@ import torch  # noqa: E402
 
 import moe_inputs as mi  # noqa: E402
 
-METRIC = "fused_moe us/call (backbone a8w4 decode, M=768)"
-SWEEP = mi.TOKENS["backbone"]
+# decode sweep of each workload's geometry (the pages' token buckets)
+SWEEP = {"backbone": mi.TOKENS["backbone"], "draft": mi.TOKENS["draft"], "ep": mi.TOKENS["ep"],
+         "a16w4_384": mi.TOKENS["a16w4"], "a16w4_385": mi.TOKENS["a16w4"], "zipf": []}
 L2_FLUSH_BYTES = 256 << 20
 
 
-def recorded_traffic(kernel: str, M: int):
+WORKLOADS = {
+    # --config name: (geometry, routing, description)
+    "backbone": ("backbone", "uniform", "DeepSeek-V4.1-Flash TP4 backbone MoE a8w4: H=5120, "
+                 "I=576 padded to 640, 384 experts, top-6, uniform routing"),
+    "draft": ("draft", "uniform", "DeepSeek-V4.1-Flash TP4 draft MoE a8w4: H=5120, I=576 "
+              "padded to 640, 128 experts, top-3, uniform routing"),
+    "ep": ("ep", "uniform", "DeepSeek-V4.1-Flash expert-parallel shard a8w4: H=5120, I=2304, "
+           "96 local of 384 experts, top-6, uniform routing"),
+    "a16w4_384": ("a16w4_384", "uniform", "DeepSeek-V4.1-Flash a16w4: H=5120, I=768, 384 "
+                  "experts, top-6, uniform routing"),
+    "a16w4_385": ("a16w4_385", "uniform", "DeepSeek-V4.1-Flash a16w4: H=5120, I=768, 385 "
+                  "experts, top-7 with the fused shared expert 384"),
+    "zipf": ("backbone", "zipf", "DeepSeek-V4.1-Flash TP4 backbone MoE a8w4: H=5120, I=576 "
+             "padded to 640, 384 experts, top-6, Zipf(1.2) routing"),
+}
+
+
+def metric_name(M: int, config: str = "backbone") -> str:
+    geo = WORKLOADS[config][0]
+    variant = "a16w4" if mi.SHAPES[geo].a16 else "a8w4"
+    label = config if config.startswith("a16w4") else f"{config} {variant}"
+    return f"fused_moe us/call ({label}, M={M})"
+
+
+def launches_per_call(M: int, topk: int) -> int:
+    """Kernels one fused call launches: up to 256 routes the sort and the
+    gather are one launch; up to 8192 routes the sort is one CTA group,
+    above it a count and a scatter launch; then stage 1, stage 2, finalise."""
+    R = M * topk
+    if R == 0:
+        return 0
+    front = 1 if R <= 256 else (2 if R <= 8192 else 3)
+    return front + 3
+
+
+def recorded_traffic(kernel: str, M: int, config: str = "backbone"):
     """DRAM bytes per launch of `kernel` from the committed ncu capture of the
     bench workload, or None when the capture is for another kernel or
     workload, or the kernel sources changed since it was taken (the record
@@ -57,7 +101,7 @@ def recorded_traffic(kernel: str, M: int):
         rec = json.load(open(path))
     except (OSError, ValueError):
         return None
-    if rec.get("kernel") != kernel or M != 768:
+    if rec.get("kernel") != kernel or M != 768 or config != "backbone":
         return None
     h = hashlib.sha256()
     for f in rec.get("source_files", []):
@@ -71,6 +115,7 @@ def recorded_traffic(kernel: str, M: int):
 
 
 def peaks():
+    """(HBM GB/s, BF16 dense TFLOP/s burst, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
@@ -108,9 +153,14 @@ def work_model(shape, ids, M):
     Et = int(torch.unique(valid).numel())
     w1_e = 2 * Ip * (H // 2 + H // 32)
     w2_e = H * (Ip // 2 + Ip // 32)
-    s1 = Et * w1_e + R * H * (1 + 1 / 32) + R * Ip * (1 + 1 / 32)
-    s2 = Et * w2_e + R * Ip * (1 + 1 / 32) + M * H * 4
-    call = Et * (w1_e + w2_e) + M * H * 2 * 2 + 2 * R * Ip * (1 + 1 / 32)
+    act = 2 if shape.a16 else 1 + 1 / 32          # bytes per activation / intermediate element
+    # stage 1 reads the weights of the touched experts and each token's
+    # (quantised) row once, and writes the intermediate of every route;
+    # stage 2 reads the weights and the intermediate and adds into the
+    # FP32 accumulator
+    s1 = Et * w1_e + M * H * act + R * Ip * act
+    s2 = Et * w2_e + R * Ip * act + M * H * 4
+    call = Et * (w1_e + w2_e) + M * H * 2 * 2 + 2 * R * Ip * act
     flops = 2.0 * R * (2 * Ip * H + H * Ip)
     return dict(R=R, experts_touched=Et, stage1_bytes=s1, stage2_bytes=s2, call_bytes=call,
                 flops=flops)
@@ -165,20 +215,29 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def _touched(case, shape):
+    flat = case.topk_ids.reshape(-1)
+    return torch.unique(flat[(flat >= 0) & (flat < shape.E)]).tolist()
+
+
+def oracle_slice(case, shape, experts):
+    """One FP64 oracle run over every route of `experts`; returns seconds."""
+    from oracle import moe as om
+    t0 = time.perf_counter()
+    om.fused_moe(case.x, case.topk_ids, case.topk_weights, case.w1, case.w1_scale,
+                 case.w2, case.w2_scale, shape.E, a16=shape.a16, experts=experts)
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(case, shape, budget_s: float = 12.0):
     """Time the FP64 oracle on a bounded slice (whole experts) of the call and
     scale to the full call by the touched-expert count."""
-    from oracle import moe as om
-    flat = case.topk_ids.reshape(-1)
-    touched = torch.unique(flat[(flat >= 0) & (flat < shape.E)]).tolist()
+    touched = _touched(case, shape)
     done, t_used = 0, 0.0
     chunk = 4
     while done < len(touched) and t_used < budget_s:
         sel = touched[done:done + chunk]
-        t0 = time.perf_counter()
-        om.fused_moe(case.x, case.topk_ids, case.topk_weights, case.w1, case.w1_scale,
-                     case.w2, case.w2_scale, shape.E, a16=shape.a16, experts=sel)
-        t_used += time.perf_counter() - t0
+        t_used += oracle_slice(case, shape, sel)
         done += len(sel)
     est_us = t_used / done * len(touched) * 1e6
     return {"value": round(est_us, 1), "unit": "us/call", "cores": os.cpu_count(),
@@ -189,32 +248,115 @@ def cpu_baseline(case, shape, budget_s: float = 12.0):
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores.
+    A whole call of the bench workload takes the oracle tens of seconds, so
+    each step runs the oracle on the same fixed slice of the call (the first
+    `slice` touched experts, every route of each); ms_per_step is the time a
+    step really took, and value is the per-call time extrapolated from the
+    slice by the touched-expert count (marked so in the line)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    shape = mi.SHAPES["backbone"]
-    case = mi.make_case("backbone", args.M)
+    geo, routing, _ = WORKLOADS[args.config]
+    shape = mi.SHAPES[geo]
+    case = mi.make_case(geo, args.M, routing=routing)
+    touched = _touched(case, shape)
+    # size the slice so that warm-up + timed steps take about args.ref_budget
+    # seconds per step at most (the first probe step sets the rate)
+    probe = oracle_slice(case, shape, touched[:4]) / 4
+    n_slice = int(max(1, min(len(touched), args.ref_budget / max(probe, 1e-6))))
+    sl = touched[:n_slice]
     for _ in range(args.warmup):
-        cpu_baseline(case, shape, budget_s=1.0)
-    budget = max(1.0, min(args.ref_budget, 150.0 / (args.steps + args.warmup)))
-    vals = [cpu_baseline(case, shape, budget_s=budget) for _ in range(args.steps)]
-    v = statistics.mean(x["value"] for x in vals)
-    cb = dict(vals[-1])
-    cb["value"] = round(v, 1)
-    line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/call",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(v / 1000, 3), "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": config_dict(args.M, world), "cpu_baseline": cb,
+        oracle_slice(case, shape, sl)
+    t_steps = [oracle_slice(case, shape, sl) for _ in range(args.steps)]
+    step_s = statistics.mean(t_steps)
+    v = step_s * len(touched) / n_slice * 1e6
+    cb = {"value": round(v, 1), "unit": "us/call", "cores": os.cpu_count(), "kind": "oracle",
+          "sample": (f"FP64 numpy oracle on {n_slice} of the {len(touched)} touched experts "
+                     f"(all their routes) of the M={args.M} call per step, "
+                     f"{step_s:.2f} s per step, scaled by {len(touched)}/{n_slice}; "
+                     "BLAS threads = host cores")}
+    line = {"impl": "reference", "metric": metric_name(args.M, args.config),
+            "value": round(v, 1),
+            "unit": "us/call", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_s * 1000, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": config_dict(args.M, world, args.config), "cpu_baseline": cb,
+            "value_extrapolated": {"from_experts": n_slice, "of_experts": len(touched),
+                                   "measured_s_per_step": round(step_s, 3)},
             "e2e": {"value": round(v, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def config_dict(M, world):
-    return {"workload": f"DeepSeek-V4.1-Flash TP4 backbone MoE a8w4 decode bucket M={M}: "
-                        "H=5120, I=576 padded to 640, 384 experts, top-6, uniform routing",
-            "tokens": M, "H": 5120, "I": 576, "Ip": 640, "experts": 384, "topk": 6,
+PREFILL = (
+    # (key, geometry, tokens, routing)
+    ("zipf_a8w4_M16384", "backbone", 16384, "zipf"),
+    ("a16w4_385_M16384", "a16w4_385", 16384, "uniform"),
+)
+
+
+def measure_prefill(m, dev, stream, flush, hbm, bf16, backbone_layer, backbone_weights,
+                    steps: int = 10):
+    """The prefill buckets of the metric: whole-call graph replays with L2
+    flushed before each, µs/call (median), TFLOP/s and the fractions of the
+    MMA peak, of HBM and of the binding roofline."""
+    res = {}
+    e_s = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    for key, name, M, routing in PREFILL:
+        shape = mi.SHAPES[name]
+        if name == "backbone":
+            layer, weights = backbone_layer, backbone_weights
+        else:
+            weights = mi.make_weights(shape, mi.weight_seed(mi.CONFIG_INDEX[name]))
+            layer = m.MoeLayer(weights["w1"], weights["w1_scale"], weights["w2"],
+                               weights["w2_scale"], a16=shape.a16, device=dev)
+        case = mi.make_case(name, M, routing=routing, weights=weights)
+        x, ids, w = case.x.to(dev), case.topk_ids.to(dev), case.topk_weights.to(dev)
+        out = torch.empty(M, shape.H, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(layer.workspace_bytes(M, shape.topk), dtype=torch.uint8, device=dev)
+        g = time_graph(layer, x, ids, w, out, ws, steps, 3, flush, stream)
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e_s.record(stream)
+            g.replay()
+            e_e.record(stream)
+            e_e.synchronize()
+            ts.append(e_s.elapsed_time(e_e))
+        us = statistics.median(ts) * 1000
+        wm = work_model(shape, case.topk_ids, M)
+        peak_tf = bf16 * (1 if shape.a16 else 2)
+        t_hbm = wm["call_bytes"] / (hbm * 1e3)          # µs
+        t_mma = wm["flops"] / (peak_tf * 1e6)           # µs
+        res[key] = {
+            "workload": (f"{name} {'a16w4' if shape.a16 else 'a8w4'} M={M}, {routing} routing, "
+                         f"E={shape.E}, top-{shape.topk}, H={shape.H}, Ip={shape.Ip}"),
+            "us": round(us, 1), "tflops": round(wm["flops"] / us / 1e6, 1),
+            "mma_peak_tflops": round(peak_tf, 1),
+            "mma_peak": ("FP8 rate = 2 x measured BF16 GEMM (MEASURED_PEAKS.json bf16_tflops)"
+                         if not shape.a16 else "measured BF16 GEMM (MEASURED_PEAKS.json)"),
+            "mma_frac": round(t_mma / us, 4), "hbm_frac": round(t_hbm / us, 4),
+            "binding_frac": round(max(t_hbm, t_mma) / us, 4),
+            "binding": "mma" if t_mma >= t_hbm else "hbm",
+            "flops": wm["flops"], "bytes": int(wm["call_bytes"]),
+            "experts_touched": wm["experts_touched"], "routes": wm["R"],
+            "replays": steps}
+        del g, ws, out, x, ids, w
+        if name != "backbone":
+            del layer
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
+def config_dict(M, world, config: str = "backbone"):
+    geo, _, desc = WORKLOADS[config]
+    shp = mi.SHAPES[geo]
+    return {"workload": f"{desc}; M={M} tokens",
+            "tokens": M, "H": shp.H, "I": shp.I, "Ip": shp.Ip, "experts": shp.E,
+            "topk": shp.topk,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": "flushed (256 MiB write) before every timed step"}
 
@@ -240,10 +382,14 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--M", type=int, default=768)
+    ap.add_argument("--config", default="backbone", choices=sorted(WORKLOADS),
+                    help="workload geometry and routing (default: the backbone decode bucket)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=4.0,
+                    help="reference arm: seconds of oracle work per step (about)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -261,18 +407,19 @@ def main():
     __graft_entry__.build()
     import block_scaled_moe_sort_gb300 as m
 
-    shape = mi.SHAPES["backbone"]
-    weights = mi.make_weights(shape, mi.weight_seed(1))
+    geo, routing, _ = WORKLOADS[args.config]
+    shape = mi.SHAPES[geo]
+    weights = mi.make_weights(shape, mi.weight_seed(mi.CONFIG_INDEX[geo]))
     layer = m.MoeLayer(weights["w1"], weights["w1_scale"], weights["w2"], weights["w2_scale"],
-                       device=dev)
-    case = mi.make_case("backbone", args.M, weights=weights)
+                       a16=shape.a16, device=dev)
+    case = mi.make_case(geo, args.M, routing=routing, weights=weights)
     x, ids, w = case.x.to(dev), case.topk_ids.to(dev), case.topk_weights.to(dev)
     M, k = args.M, shape.topk
     out = torch.empty(M, shape.H, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(layer.workspace_bytes(M, k), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    hbm, _, peak_kind = peaks()
+    hbm, bf16, peak_kind = peaks()
     wm = work_model(shape, case.topk_ids, M)
 
     with torch.cuda.stream(stream):
@@ -335,8 +482,8 @@ def main():
         # ---- decode sweep of the same geometry
         sweep = {}
         if not args.no_sweep:
-            for Ms in SWEEP:
-                c = mi.make_case("backbone", Ms, weights=weights)
+            for Ms in SWEEP[args.config]:
+                c = mi.make_case(geo, Ms, routing=routing, weights=weights)
                 xs, ids_s, w_s = c.x.to(dev), c.topk_ids.to(dev), c.topk_weights.to(dev)
                 o_s = torch.empty(Ms, shape.H, dtype=torch.bfloat16, device=dev)
                 ws_s = torch.empty(layer.workspace_bytes(Ms, k), dtype=torch.uint8, device=dev)
@@ -380,6 +527,11 @@ def main():
                                    "gbs": round(nbytes / us / 1e3, 1),
                                    "hbm_frac": round(nbytes / us / 1e3 / hbm, 3)}
 
+    prefill = {}
+    if not args.no_prefill:
+        with torch.cuda.stream(stream):
+            prefill = measure_prefill(m, dev, stream, flush, hbm, bf16, layer, weights)
+
     # ---- roofline of the dominant kernel
     dom = max(("stage1_gemm", "stage2_gemm"), key=lambda kk: kmean[kk])
     dom_bytes = wm["stage1_bytes"] if dom == "stage1_gemm" else wm["stage2_bytes"]
@@ -387,16 +539,17 @@ def main():
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
             "unit": "GB/s", "frac": round(achieved / hbm, 4),
-            "traffic": recorded_traffic(dom, M),
+            "traffic": recorded_traffic(dom, M, args.config),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
             "algorithmic_bytes": int(dom_bytes), "kernel_us": round(dom_ms * 1000, 2)}
 
     line = {
-        "metric": METRIC, "value": round(call_us, 2), "unit": "us/call", "n_gpus": world,
+        "metric": metric_name(M, args.config), "value": round(call_us, 2), "unit": "us/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 x mxfp4 (fp32 accumulate)",
-        "data": "synthetic (seeded, random-init weights)", "config": config_dict(M, world),
+        "scaling": "weak", "vs_baseline": None, "dtype": ("bf16 x mxfp4 (fp32 accumulate)" if shape.a16
+                  else "fp8e4m3 x mxfp4 (fp32 accumulate)"),
+        "data": "synthetic (seeded, random-init weights)", "config": config_dict(M, world, args.config),
         "tflops": round(wm["flops"] / call_us / 1e6, 2),
         "call_hbm_frac": round(wm["call_bytes"] / call_us / 1e3 / hbm, 4),
         "kernels_us": {kk: round(v * 1000, 2) for kk, v in kmean.items()},
@@ -404,7 +557,7 @@ def main():
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call",
                 "h2d_bytes_per_step": int(x.numel() * 2 + ids.numel() * 4 + w.numel() * 4),
                 "d2h_bytes_per_step": int(out.numel() * 2)},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": launches_per_call(M, k) * args.steps,
         "clocks": clocks,
         "work": wm,
     }
@@ -412,6 +565,8 @@ def main():
         line["sweep"] = sweep
     if router:
         line["router"] = router
+    if prefill:
+        line["prefill"] = prefill
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, shape)
     if rank == 0:

@@ -22,6 +22,7 @@ __all__ = [
     "moe_prepack_scales_mx", "moe_prepack_weights_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
     "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS", "fused_moe_a8w4_noalloc",
+    "moe_noalloc_status",
 ]
 
 HEADER = os.path.join(_build.ROOT, "include", "moe_mx.h")
@@ -80,6 +81,7 @@ _SIGS = {
     "fused_moe_a8w4_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
                                         _c_int, _c_void_p, _c_void_p]),
+    "moe_noalloc_status": (_c_int, [_c_void_p, _c_void_p]),
     "moe_profile_enable": (_c_int, [_c_int]),
     "moe_profile_collect": (_c_int, [ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_int32)]),
@@ -335,6 +337,17 @@ def fused_moe_a8w4_noalloc(x, topk_ids, topk_weights, w1, w1_scale_packed, w2,
         _ptr(w2), _ptr(w2_scale_packed), E, Ip, _ptr(out), _stream(stream))
     _check("fused_moe_a8w4_noalloc", code)
     return out
+
+
+def moe_noalloc_status(device="cuda", stream=None) -> tuple:
+    """(decoded device status, padded route count) of the last
+    fused_moe_a8w4_noalloc call on `device`, read through
+    moe_noalloc_status (synchronises the stream)."""
+    st = torch.zeros(4, dtype=torch.int32, device=device)
+    _check("moe_noalloc_status", lib().moe_noalloc_status(_ptr(st), _stream(stream)))
+    torch.cuda.synchronize(st.device)
+    word, padded = st.cpu().tolist()[:2]
+    return int(lib().moe_decode_device_status(word)), int(padded)
 
 
 def moe_profile_enable(enable: bool = True) -> None:

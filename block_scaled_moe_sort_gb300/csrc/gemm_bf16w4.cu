@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       constexpr int kPrefetch = 8;
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t armed_mask = 0, armed_par = 0;   // stages armed, parity of their last arming
       Seq16 cur;
       cur.init(a, total_tiles, P, BN);
 #ifdef MOE_TIMELINE
@@ -251,6 +252,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           if (!ok) { abort_flag = 1; break; }
           uint8_t* sb = stage_ptr(stage);
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+          armed_mask |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
 #ifdef MOE_TIMELINE
           if (tl_first) { MOE_TL(3 + a.stage, 2); tl_first = 0; }
 #endif
@@ -267,6 +270,11 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         }
         cur.next(a, total_tiles, P, BN);
       }
+      // Copies still in flight into shared memory must land before the CTA
+      // exits: normally every armed stage was consumed, so these return at
+      // once; after an abort they wait (bounded) for the TMA.
+      for (int s = 0; s < C::kStages; ++s)
+        if ((armed_mask >> s) & 1u) mbar_wait(&full_bar[s], (armed_par >> s) & 1u, a.status);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue

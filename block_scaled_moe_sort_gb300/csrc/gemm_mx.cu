@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       constexpr uint32_t kWTile = kTileN * kTileK / 2;   // 8 KB
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t armed_mask = 0, armed_par = 0;   // stages armed, parity of their last arming
       uint8_t* sbase = stages;
       Seq cur;
       seq_init(cur, a, total_tiles, P, BN, kblocks);
@@ -237,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             WAIT_ADD(0);
           }
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+          armed_mask |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
 #ifdef MOE_TIMELINE
           if (tl_first) { MOE_TL(3 + a.stage, 2); tl_first = 0; }
 #endif
@@ -259,6 +262,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
         }
         seq_next(cur, a, total_tiles, P, BN);
       }
+      // Copies still in flight into shared memory must land before the CTA
+      // exits: normally the MMA thread consumed every armed stage, so these
+      // return at once; after an abort they wait (bounded) for the TMA.
+      for (int s = 0; s < C::kStages; ++s)
+        if ((armed_mask >> s) & 1u) mbar_wait(&full_bar[s], (armed_par >> s) & 1u, a.status);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue

@@ -7,8 +7,21 @@
 #pragma once
 #include <cstdint>
 #include "common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
+
+// Expert of route block m. The sort writes ids in [0, E) for every block
+// below the padded route count; any other value means a corrupted route
+// list: it is reported through the status word (kDevBadExpert) and replaced
+// by expert 0, so no weight access leaves the weight arrays.
+template <class Args>
+__device__ __forceinline__ int block_expert_checked(const Args& a, int m) {
+  const int e = __ldg(a.block_expert + m);
+  if (static_cast<unsigned>(e) < static_cast<unsigned>(a.E)) return e;
+  if (a.status) atomicOr(a.status, kDevBadExpert);
+  return 0;
+}
 
 template <class Args>
 __device__ __forceinline__ void tile_coords(int t, const Args& a, int& m_blk, int& n_tile) {
@@ -45,16 +58,16 @@ struct TileSeq {
   __device__ __forceinline__ void init(const Args& a, int total, int P, int bn) {
     t = blockIdx.x;
     valid = find(t, m_blk, n_tile, a, total, P, bn);
-    e = valid ? __ldg(a.block_expert + m_blk) : -1;
+    e = valid ? block_expert_checked(a, m_blk) : -1;
     nt = t + gridDim.x;
     nvalid = valid && find(nt, nm, nn, a, total, P, bn);
-    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+    ne = nvalid ? block_expert_checked(a, nm) : -1;
   }
   __device__ __forceinline__ void next(const Args& a, int total, int P, int bn) {
     t = nt; m_blk = nm; n_tile = nn; e = ne; valid = nvalid;
     nt = t + gridDim.x;
     nvalid = valid && find(nt, nm, nn, a, total, P, bn);
-    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+    ne = nvalid ? block_expert_checked(a, nm) : -1;
   }
 };
 
@@ -107,17 +120,17 @@ struct SplitSeq {
     if (parts > 1) { S = parts; wg = W * G; U = wg + r * parts; } else { S = 1; wg = T; U = T; }
     t = blockIdx.x;
     valid = locate(t, m_blk, n_tile, kb0, kb1, slot, a);
-    e = valid ? __ldg(a.block_expert + m_blk) : -1;
+    e = valid ? block_expert_checked(a, m_blk) : -1;
     nt = t + gridDim.x;
     nvalid = valid && locate(nt, nm, nn, nkb0, nkb1, nslot, a);
-    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+    ne = nvalid ? block_expert_checked(a, nm) : -1;
   }
   __device__ __forceinline__ void next(const Args& a) {
     t = nt; m_blk = nm; n_tile = nn; e = ne; kb0 = nkb0; kb1 = nkb1; slot = nslot;
     valid = nvalid;
     nt = t + gridDim.x;
     nvalid = valid && locate(nt, nm, nn, nkb0, nkb1, nslot, a);
-    ne = nvalid ? __ldg(a.block_expert + nm) : -1;
+    ne = nvalid ? block_expert_checked(a, nm) : -1;
   }
 };
 

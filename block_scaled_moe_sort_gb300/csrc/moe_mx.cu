@@ -239,6 +239,7 @@ const char* moe_status_string(moe_status_t s) {
     case MOE_ERR_ALIGNMENT: return "pointer not 256-byte aligned";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side check failed (expert id out of range)";
   }
   return "unknown status";
 }
@@ -285,6 +286,10 @@ moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t
 moe_status_t moe_router_topk(const float* logits, int M, int E, int ld, int topk, int shared_id,
                              int32_t* topk_ids, float* topk_weights, moe_stream_t stream) {
   if (M < 0 || E <= 0 || ld < E || topk < 1 || topk > E) return MOE_ERR_INVALID_ARG;
+  // a shared expert is an extra expert after the routed ones: an id among
+  // them would double-count a pick, one beyond the sort's range would be
+  // dropped silently
+  if (shared_id >= 0 && (shared_id < E || shared_id >= kMaxExperts)) return MOE_ERR_INVALID_ARG;
   if (E > kMaxExperts || topk + (shared_id >= 0 ? 1 : 0) > kMaxTopk) return MOE_ERR_UNSUPPORTED;
   if (M > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
   if (M > 0 && (!aligned(logits) || !aligned(topk_ids) || !aligned(topk_weights)))
@@ -412,7 +417,9 @@ moe_status_t moe_debug_wait_selftest(int32_t* status, int timeout_us, moe_stream
 }
 
 moe_status_t moe_decode_device_status(int32_t status_word) {
-  return (status_word & kDevTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
+  if (status_word & kDevTimeout) return MOE_ERR_TIMEOUT;
+  if (status_word & kDevBadExpert) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
 }
 
 }  // extern "C"

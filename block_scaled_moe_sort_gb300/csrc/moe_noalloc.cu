@@ -65,8 +65,24 @@ extern "C" moe_status_t fused_moe_a8w4_noalloc(const void* x, const int32_t* top
   void* ws = nullptr;
   if (moe::noalloc_ws_current_device(&ws) != cudaSuccess) return MOE_ERR_CUDA;
   // Nothing in the workspace has to start at zero: every call's kernels
-  // write what they read (the sort resets the status word and the route
-  // lists, the gather zeroes the accumulator).
+  // write what they read (the front kernel or the sort resets the status
+  // word and writes the route lists, the stage-1 GEMM zeroes the
+  // accumulator, the front kernel or the gather zeroes the split buffers).
   return fused_moe_a8w4(x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale, E,
                         Ip, out, ws, MOE_NOALLOC_WORKSPACE_BYTES, stream);
+}
+
+extern "C" moe_status_t moe_noalloc_status(int32_t* status_out, moe_stream_t stream) {
+  if (!status_out) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(status_out) % 16 != 0) return MOE_ERR_ALIGNMENT;
+  void* ws = nullptr;
+  if (moe::noalloc_ws_current_device(&ws) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_ws_layout_t L;
+  // the status words sit at the same offset for every shape (the first
+  // region of the layout); any valid shape gives it
+  if (fused_moe_workspace_layout(1, 128, 128, 1, 1, 0, &L) != MOE_OK) return MOE_ERR_CUDA;
+  const cudaError_t e = cudaMemcpyAsync(status_out, static_cast<uint8_t*>(ws) + L.status_off,
+                                        4 * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

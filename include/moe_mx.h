@@ -58,7 +58,9 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,    /* workspace smaller than the *_workspace_bytes size */
   MOE_ERR_ALIGNMENT = 4,    /* a pointer not 256-byte aligned */
   MOE_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed */
-  MOE_ERR_TIMEOUT = 6       /* reported by moe_decode_device_status */
+  MOE_ERR_TIMEOUT = 6,      /* reported by moe_decode_device_status */
+  MOE_ERR_DEVICE_CHECK = 7  /* reported by moe_decode_device_status: a route block
+                               reached a GEMM with an expert id outside [0, E) */
 } moe_status_t;
 
 /* Static text for a status code (never NULL). */
@@ -111,7 +113,9 @@ moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M,
  * topk_ids int32 / topk_weights float32: [M, topk (+1 with a shared expert)],
  *   caller-allocated device memory, fully written.
  * Errors (before any launch): MOE_ERR_INVALID_ARG for M < 0, E < 1, ld < E,
- * topk outside [1, E] or a NULL pointer with M > 0; MOE_ERR_UNSUPPORTED for
+ * topk outside [1, E], a shared_id >= 0 outside [E, 512) (a shared expert
+ * comes after the E routed experts) or a NULL pointer with M > 0;
+ * MOE_ERR_UNSUPPORTED for
  * E > 512 or more than 16 output columns; MOE_ERR_ALIGNMENT for pointers not
  * 256-byte aligned. M == 0 launches nothing.
  */
@@ -256,11 +260,16 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any
- * stream capture on the device. All calls share the one array and it keeps
+ * stream capture on the device. The cached address is that of the device
+ * context current at the first call: after cudaDeviceReset on a device this
+ * entry point (and moe_noalloc_status) must not be used on that device
+ * again in the same process. All calls share the one array and it keeps
  * the previous call's contents (no part of it needs to start at zero), so
  * calls that can overlap on the GPU (different streams, or different host
  * threads) race on it: serialise them. Arguments, limits, layouts and errors
- * are otherwise those of fused_moe_a8w4.
+ * are otherwise those of fused_moe_a8w4; the device status words that
+ * fused_moe_a8w4 leaves in the caller's workspace are read with
+ * moe_noalloc_status.
  */
 #define MOE_NOALLOC_WORKSPACE_BYTES (16u << 20)
 moe_status_t fused_moe_a8w4_noalloc(const void* x, const int32_t* topk_ids,
@@ -268,6 +277,17 @@ moe_status_t fused_moe_a8w4_noalloc(const void* x, const int32_t* topk_ids,
                                     const uint8_t* w1, const uint8_t* w1_scale,
                                     const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
                                     void* out, moe_stream_t stream);
+
+/* moe_noalloc_status: the device-side status of the last
+ * fused_moe_a8w4_noalloc call on the current device. Enqueues, on `stream`,
+ * a device-to-device copy of the scratch array's status words (int32[4]:
+ * [0] device status bits, decoded by moe_decode_device_status; [1] the
+ * padded route count P) into status_out, a caller-owned device buffer of 16
+ * bytes, 16-byte aligned. Allocates nothing. Read it after the call it
+ * reports on has completed on that stream (same stream order, or a sync).
+ * MOE_ERR_INVALID_ARG for a NULL pointer, MOE_ERR_ALIGNMENT for a
+ * misaligned one, MOE_ERR_CUDA if the copy cannot be enqueued. */
+moe_status_t moe_noalloc_status(int32_t* status_out, moe_stream_t stream);
 
 /* --------------------------------------------------------- kernel timing
  * For benchmarks and profiling. While enabled, every fused_moe_* call records
@@ -286,7 +306,10 @@ moe_status_t moe_profile_enable(int enable);
 moe_status_t moe_profile_collect(double* kernel_ms, int32_t* n_calls);
 
 /* Decode the status word copied from the workspace (host value) into a
- * moe_status_t: MOE_OK, or MOE_ERR_TIMEOUT if a device wait gave up. */
+ * moe_status_t: MOE_OK; MOE_ERR_TIMEOUT if a device wait gave up (bit 0);
+ * MOE_ERR_DEVICE_CHECK if a GEMM met a route block whose expert id was
+ * outside [0, E) (bit 1; it then used expert 0 for that block, so no access
+ * left the weight arrays, and the output is not valid). */
 moe_status_t moe_decode_device_status(int32_t status_word);
 
 /* Self-test of the device-side failure reporting: one kernel waits, with the

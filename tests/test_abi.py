@@ -28,8 +28,8 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(7):
-        assert L.moe_status_string(code)
+    for code in range(8):
+        assert L.moe_status_string(code) != b"unknown status"
     assert L.moe_status_string(3) == b"workspace too small"
 
 
@@ -100,6 +100,9 @@ def test_sort_and_quant_reject_bad_arguments(L):
 def test_device_status_decoding(L):
     assert L.moe_decode_device_status(0) == 0
     assert L.moe_decode_device_status(1) == 6
+    assert L.moe_decode_device_status(2) == 7
+    assert L.moe_decode_device_status(3) == 6     # a timeout is reported first
+    assert L.moe_status_string(7).startswith(b"device-side check")
 
 
 def test_router_rejects_bad_arguments_on_host(L):
@@ -111,6 +114,9 @@ def test_router_rejects_bad_arguments_on_host(L):
     assert call(lg=None) == 1
     assert call(E=600, ld=600) == 2            # > 512 experts
     assert call(k=16, shared=384) == 2         # 17 output columns
+    assert call(shared=0) == 1                 # a routed expert as the shared one
+    assert call(shared=383) == 1
+    assert call(shared=512) == 1               # beyond the sort's expert range
     assert call(w=FAKE + 4) == 4               # misaligned
     assert call(M=0, lg=None, ids=None, w=None) == 0   # empty call, no launch
 
@@ -126,6 +132,11 @@ def test_explicit_block_m_validation(L):
     args = [FAKE, FAKE, FAKE, 4, 256, 2, FAKE, FAKE, FAKE, FAKE, 8, 128, FAKE, FAKE, 1 << 40]
     assert L.fused_moe_a8w4_bm(*args, 24, None) == 2
     assert L.fused_moe_a16w4_bm(*args, 512, None) == 2
+
+
+def test_noalloc_status_rejects_bad_arguments_on_host(L):
+    assert L.moe_noalloc_status(None, None) == 1
+    assert L.moe_noalloc_status(FAKE + 4, None) == 4
 
 
 def test_wait_selftest_rejects_bad_arguments_on_host(L):

@@ -6,8 +6,12 @@ boundary checks and concentrated routing, expert-parallel shard, a16w4
 384-top6 and 385-top7 with the fused shared expert at decode and prefill
 sizes, Zipf prefill stress) are
 compared on every route of a seeded sample of tokens, at the sizes and in the
-launch configuration the benchmark uses. Workspace and output are poisoned
-(0xFF) before each call, so anything left unwritten shows up.
+launch configuration the benchmark uses. At M=16384 the stage-one
+intermediate of every route of three whole experts is compared as well: the
+most loaded expert, the one whose route blocks open the last wave of
+stage-one tiles, and the last non-empty expert; the sampled tokens include
+tokens of each of them. Workspace and output are poisoned (0xFF) before each
+call, so anything left unwritten shows up.
 """
 import numpy as np
 import pytest
@@ -15,7 +19,8 @@ import torch
 
 import block_scaled_moe_sort_gb300 as m
 import moe_inputs as mi
-from moe_check import compare, layer_for, sample_tokens
+from moe_check import compare, layer_for, sample_tokens, tokens_of_expert
+from oracle import moe as om
 
 pytestmark = pytest.mark.gpu
 
@@ -91,10 +96,42 @@ def test_backbone_concentrated_routing(cuda_lib):
     print(compare(case, layer, False, tokens=tok))
 
 
-@pytest.mark.parametrize("M", [1, 16, 1024, 16384])
+def _prefill_experts(case, layer):
+    """(experts to check whole, tokens to compare) for a prefill case: the
+    most loaded expert, the expert of the route block that opens the last
+    wave of stage-one tiles (CTA slots = SMs x 2 at route blocks <= 128),
+    and the last non-empty expert; 24 tokens of each of the latter two, 16
+    of the first and 16 drawn from all tokens."""
+    M, k = case.M, case.topk_ids.shape[1]
+    bm = layer.workspace_layout(M, k)["block_m"]
+    srt = om.moe_sort(case.topk_ids, case.topk_weights, layer.E, bm)
+    cnt = srt.expert_cnt
+    hot = int(np.argmax(cnt))
+    last = int(np.nonzero(cnt)[0][-1])
+    n_tiles = 2 * layer.Ip // 128
+    slots = torch.cuda.get_device_properties(0).multi_processor_count * 2
+    tiles = srt.num_padded // bm * n_tiles
+    first_last_wave = (tiles // slots) * slots
+    if first_last_wave >= tiles:
+        first_last_wave = max(tiles - slots, 0)
+    wave = int(srt.block_expert[first_last_wave // n_tiles])
+    experts = sorted({hot, last, wave})
+    tok = np.unique(np.concatenate([
+        tokens_of_expert(case, hot, 16, 1), tokens_of_expert(case, wave, 24, 2),
+        tokens_of_expert(case, last, 24, 3), sample_tokens(M, 16, 4)]))
+    return experts, tok
+
+
+@pytest.mark.parametrize("M", [1, 16, 1024])
 def test_expert_parallel_shard(cuda_lib, M):
     layer, case, tok = _config_case("ep", M)
     print(compare(case, layer, False, tokens=None if M <= 16 else tok))
+
+
+def test_expert_parallel_shard_prefill_whole_experts(cuda_lib):
+    layer, case, _ = _config_case("ep", 16384)
+    experts, tok = _prefill_experts(case, layer)
+    print(compare(case, layer, False, tokens=tok, whole_experts=experts))
 
 
 @pytest.mark.parametrize("name", ["a16w4_384", "a16w4_385"])
@@ -104,12 +141,21 @@ def test_a16w4(cuda_lib, name, M):
     print(compare(case, layer, True, tokens=None if M <= 12 else tok))
 
 
-@pytest.mark.parametrize("name,M", [("a16w4_384", 4096), ("a16w4_385", 16384)])
-def test_a16w4_prefill(cuda_lib, name, M):
-    # route blocks of 64 and 128 rows and the grouped stage-2 tile walk (the
-    # BF16 intermediate is larger than 32 MB) on the a16w4 geometries
-    layer, case, tok = _config_case(name, M)
+def test_a16w4_prefill_4096(cuda_lib):
+    # route blocks of 64 rows and the grouped stage-2 tile walk (the BF16
+    # intermediate is larger than 32 MB) on the 384-expert a16w4 geometry
+    layer, case, tok = _config_case("a16w4_384", 4096, n_tok=32)
     print(compare(case, layer, True, tokens=tok))
+
+
+def test_a16w4_shared_expert_prefill_whole_experts(cuda_lib):
+    # 385 experts top-7 at M=16384: the shared expert (id 384) holds 16384
+    # routes, the most loaded segment, and is the last expert in the list
+    layer, case, _ = _config_case("a16w4_385", 16384)
+    experts, tok = _prefill_experts(case, layer)
+    assert 384 in experts
+    experts = sorted(set(experts) | {383})
+    print(compare(case, layer, True, tokens=tok, whole_experts=experts))
 
 
 def test_zipf_prefill_stress(cuda_lib):
@@ -118,4 +164,5 @@ def test_zipf_prefill_stress(cuda_lib):
     case = mi.make_case("backbone", 16384, routing="zipf", weights=w)
     counts = np.bincount(case.topk_ids.reshape(-1).numpy(), minlength=384)
     assert counts.max() > 20 * np.median(counts)
-    print(compare(case, layer, False, tokens=sample_tokens(16384, 8, 4)))
+    experts, tok = _prefill_experts(case, layer)
+    print(compare(case, layer, False, tokens=tok, whole_experts=experts))

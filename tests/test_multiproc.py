@@ -65,3 +65,36 @@ def test_reference_arm_runs_on_rank0_only():
                         "--steps", "1", "--warmup", "3"], env=env, capture_output=True,
                        text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_line_fits_its_own_clock():
+    # each step times the oracle on a fixed slice of the call: the line's
+    # steps x ms_per_step must fit in the process's wall time, and the
+    # per-call value is marked as extrapolated from that slice
+    import time
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    t0 = time.time()
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "3", "--M", "12", "--ref-budget", "0.3"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    wall = time.time() - t0
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    assert line["steps"] * line["ms_per_step"] / 1000 < wall
+    ex = line["value_extrapolated"]
+    assert 1 <= ex["from_experts"] <= ex["of_experts"]
+    assert line["value"] == pytest.approx(
+        ex["measured_s_per_step"] * ex["of_experts"] / ex["from_experts"] * 1e6, rel=0.01)
+    assert line["metric"].endswith("M=12)")
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_launch_count_and_metric_follow_the_workload():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.launches_per_call(0, 6) == 0
+    assert bench.launches_per_call(42, 6) == 4          # 252 routes: one front launch
+    assert bench.launches_per_call(768, 6) == 5         # sort, gather, 2 GEMMs, finalise
+    assert bench.launches_per_call(16384, 6) == 6       # count + scatter sort
+    assert bench.metric_name(16384).endswith("M=16384)")

@@ -51,6 +51,13 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_lib, name, Ms):
                                        layer.w2_scale, layer.E, layer.Ip, out=out)
         torch.cuda.synchronize()
         _check_close(got, want)
+        # the device status of the call just made, read from the library's
+        # scratch: no wait gave up, and the padded route count is the one
+        # the workspace entry point computed
+        code, padded = m.moe_noalloc_status()
+        assert code == 0
+        lay = layer.workspace_layout(M, mi.SHAPES[name].topk)
+        assert 0 < padded <= lay["p_max"] and padded % lay["block_m"] == 0
 
 
 def test_noalloc_refuses_shapes_that_do_not_fit(cuda_lib):
