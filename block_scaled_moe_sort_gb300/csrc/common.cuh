@@ -13,6 +13,9 @@ constexpr int kMaxTopk = 16;
 constexpr int kSplitSlots = 320;
 // Up to this many routes the call's front (sort + gather) is one launch.
 constexpr int kFrontMaxRoutes = 256;
+// Upper bound of the static shared memory of a GEMM CTA (mbarriers, flags
+// and the local route layout of kMaxExperts + 1 ints).
+constexpr int kStaticSmem = 512 + 4 * (kMaxExperts + 1);
 
 // Stage-2 tile walk: feature tiles per group (route-block major inside a
 // group). Once the intermediate no longer fits comfortably in L2, every

@@ -28,6 +28,7 @@
 // atom, and two 128-byte swizzle atoms of BF16 activations.
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include "common.cuh"
@@ -68,6 +69,8 @@ struct Bf16Args {
   int n_tiles;
   int num_blocks;
   int n_group_log2;            // stage 2: log2 of the feature tiles per walk group
+  int local;                   // derive the route layout from topk_ids (decode sizes)
+  const int32_t* topk_ids;
   const int32_t* sorted_route;
   const float* sorted_w;
   const int32_t* block_expert;
@@ -86,11 +89,15 @@ __host__ __device__ constexpr int pow2_cols(int c) {
 template <int BN>
 struct Cfg16 {
   // Small route blocks run two CTAs per SM so that two MMA issuers and two
-  // converter groups share the SM. The dequantised-weight slots in TMEM are
-  // the shared-memory stages (slot = stage), so one commit per k-block frees
-  // both: the converter writes slot s only after the stage's new TMA data
-  // landed, and the producer issued those loads only after the MMA that read
-  // slot s had committed. The ring depth is therefore bounded by TMEM.
+  // converter groups share the SM. Shared-memory stages (the TMA ring) and
+  // TMEM slots of dequantised weight tiles are two rings of their own
+  // depths: k-block j uses stage j % kStages and slot j % kASlots. The MMA's
+  // one commit per k-block frees both its stage and its slot; the converter
+  // writes slot j % kASlots once the stage of k-block j has landed and the
+  // MMA of k-block j - kASlots has committed. TMEM bounds the slots (3 at
+  // two CTAs per SM); shared memory bounds the stages, so at small route
+  // blocks the TMA runs up to kStages k-blocks ahead while the converters run
+  // up to kASlots ahead of the MMA.
   static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
   static constexpr int kConvWarps = kCtasPerSm == 2 ? 4 : 8;
   static constexpr int kThreads = 192 + 32 * kConvWarps;
@@ -100,18 +107,21 @@ struct Cfg16 {
   static constexpr int kBBytes = 2 * kBAtomBytes;
   // stage layout: B atoms, raw FP4 tile (64-byte swizzled), scale atom
   static constexpr int kStageBytes = (kBBytes + kRawBytes + kSfBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = BN <= 32 ? 3 : BN == 64 ? 6 : BN == 128 ? 4 : 2;
-  static constexpr int kASlots = kStages;
+  static constexpr int kASlots = BN <= 32 ? 3 : BN == 64 ? 6 : BN == 128 ? 4 : 2;
+  static constexpr int kStages = kASlots;
+  static_assert(kStages >= kASlots, "a slot is reused only after its stage was");
   static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
   static constexpr int kAccCol0 = kASlots * kACols;
   static constexpr int kTmemCols = pow2_cols(kAccCol0 + kAccBufs * BN);
   static constexpr int kLutWords = 256 * 32;
   static constexpr int kEpiFloats = 32 * (64 + 4);
-  static constexpr int kRouteBytes = 256 * 8;
+  static constexpr int kRouteBytes = BN * 8;                   // per-tile route info
   static constexpr int kSmem =
       1024 + kStages * kStageBytes + kLutWords * 4 + kEpiFloats * 4 + kRouteBytes;
   static constexpr uint32_t kTxBytes = kRawBytes + kSfBytes + kBBytes;
-  static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
+  // per SM: 228 KB, of which 1 KB is reserved per CTA; the static shared
+  // variables (barriers, the local route layout) take up to kStaticSmem
+  static_assert(kCtasPerSm * (kSmem + 1024 + kStaticSmem) <= 228 * 1024, "smem budget");
   static_assert(kAccCol0 + kAccBufs * BN <= kTmemCols && kTmemCols * kCtasPerSm <= 512,
                 "TMEM budget");
 };
@@ -143,7 +153,8 @@ __device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t s) {
   return h | (h << 16);
 }
 
-using Seq16 = TileSeq<Bf16Args>;
+using Seq16 = TileSeq<Bf16Args>;          // producer: loads each tile's expert
+using Seq16R = TileSeq<Bf16Args, false>;  // other roles
 
 template <int BN>
 __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
@@ -157,13 +168,15 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::kStages * C::kStageBytes);  // [256][32]
   float* epi = reinterpret_cast<float*>(lut + C::kLutWords);
   int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token / -1 pad
-  float* s_w = reinterpret_cast<float*>(s_tok + 256);             // [BN] routing weight
+  float* s_w = reinterpret_cast<float*>(s_tok + BN);              // [BN] routing weight
   __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
   __shared__ uint64_t a_full[C::kASlots];
   __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ uint16_t s_blk_expert[kLocalMaxBlocks];   // local layout: expert of each route block
+  __shared__ int s_nblk;                               // local layout: number of route blocks
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #ifdef MOE_WAIT_STATS
@@ -203,21 +216,29 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     tmem_alloc(&tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  // Decode sizes: the route layout is derived from topk_ids before the
+  // dependency wait (see local_block_layout), so the producer loads its first
+  // weight tiles while the previous kernel still runs.
+  if (a.local) {
+    // the epilogue's transpose buffer is free until the first tile's epilogue
+    const int nb = local_block_layout(a.topk_ids, a.M * a.topk, a.E, BN,
+                                      reinterpret_cast<int*>(epi), s_blk_expert);
+    if (threadIdx.x == 0) s_nblk = nb;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  // everything above overlaps the previous kernel; its outputs are read below
-  pdl_wait_prior();
-  if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
-  const int P = *a.num_padded;
 
   auto stage_ptr = [&](int s) { return smem + s * C::kStageBytes; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // A second cursor runs kPrefetch weight tiles ahead and prefetches them
-    // (contiguous 8 KB blocks) and their scale atoms into L2.
+    // (contiguous 8 KB blocks) and their scale atoms into L2. With the local
+    // layout the weight half of the first ring stages (packed tile and scale
+    // atom) is loaded before the dependency wait and the activation half
+    // after it.
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
@@ -225,51 +246,117 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed_mask = 0, armed_par = 0;   // stages armed, parity of their last arming
-      Seq16 cur;
-      cur.init(a, total_tiles, P, BN);
 #ifdef MOE_TIMELINE
       int tl_first = 1;
 #endif
-      Seq16 pf = cur;
-      int pf_kb = 0;
-      auto pf_step = [&]() {
-        if (!pf.valid) return;
-        const int64_t tile = (static_cast<int64_t>(pf.e) * a.n_tiles + pf.n_tile) * kblocks + pf_kb;
-        // with the tile's weight scale atoms (512 B per k-block, contiguous)
-        if (pf_kb == 0) bulk_prefetch_l2(a.sfa + tile * 512, static_cast<uint32_t>(kblocks) * 512);
-        bulk_prefetch_l2(a.w + tile * C::kRawBytes, C::kRawBytes);
-        if (++pf_kb == kblocks) {
-          pf_kb = 0;
-          pf.next(a, total_tiles, P, BN);
+      auto produce = [&](auto cur, auto expert_of, auto local_mode) {
+        constexpr bool kLocal = decltype(local_mode)::value;
+        int P;
+        if constexpr (kLocal) {
+          P = s_nblk * BN;
+        } else {
+          pdl_wait_prior();
+          if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
+          P = *a.num_padded;
         }
-      };
-      for (int i = 0; i < kPrefetch; ++i) pf_step();
-      while (cur.valid && !abort_flag) {
-        const int64_t tile0 = (static_cast<int64_t>(cur.e) * a.n_tiles + cur.n_tile) * kblocks;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          bool ok;
-          { WS_T0(); ok = mbar_wait(&empty_bar[stage], phase ^ 1, a.status); WS_ADD(0); }
-          if (!ok) { abort_flag = 1; break; }
-          uint8_t* sb = stage_ptr(stage);
+        cur.init(a, total_tiles, P, BN);
+        auto pf = cur;
+        int pf_kb = 0;
+        auto pf_skip = [&]() {
+          if (++pf_kb == kblocks) {
+            pf_kb = 0;
+            pf.next(a, total_tiles, P, BN);
+          }
+        };
+        auto pf_step = [&]() {
+          if (!pf.valid) return;
+          const int64_t tile =
+              (static_cast<int64_t>(expert_of(pf)) * a.n_tiles + pf.n_tile) * kblocks + pf_kb;
+          // with the tile's weight scale atoms (512 B per k-block, contiguous)
+          if (pf_kb == 0) bulk_prefetch_l2(a.sfa + tile * 512, static_cast<uint32_t>(kblocks) * 512);
+          bulk_prefetch_l2(a.w + tile * C::kRawBytes, C::kRawBytes);
+          pf_skip();
+        };
+        int kb = 0;
+        int64_t tile0 = 0;
+        auto set_tile = [&]() {
+          tile0 = (static_cast<int64_t>(expert_of(cur)) * a.n_tiles + cur.n_tile) * kblocks;
+          kb = 0;
+        };
+        auto arm = [&]() {
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
           armed_mask |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
 #ifdef MOE_TIMELINE
           if (tl_first) { MOE_TL(3 + a.stage, 2); tl_first = 0; }
 #endif
+        };
+        auto load_w = [&]() {
+          uint8_t* sb = stage_ptr(stage);
           tma_load_2d(sb + C::kBBytes, &tmW, &full_bar[stage], 0,
                       static_cast<int32_t>((tile0 + kb) * kTileN), pol_w);
           bulk_load(sb + C::kBBytes + C::kRawBytes, a.sfa + (tile0 + kb) * 512, 512,
                     &full_bar[stage], pol_w);
+        };
+        auto load_x = [&](int st, int kbx, int m_blk) {
+          uint8_t* sb = stage_ptr(st);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            tma_load_2d(sb + h * C::kBAtomBytes, &tmX, &full_bar[stage],
-                        kb * kTileK + h * kAtomK, cur.m_blk * BN, pol_x);
-          pf_step();
+            tma_load_2d(sb + h * C::kBAtomBytes, &tmX, &full_bar[st], kbx * kTileK + h * kAtomK,
+                        m_blk * BN, pol_x);
+        };
+        auto advance = [&](bool prefetch) {
+          if (prefetch) pf_step();
+          else if (pf.valid) pf_skip();
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+          if (++kb == kblocks) {
+            cur.next(a, total_tiles, P, BN);
+            if (cur.valid) set_tile();
+          }
+        };
+        if (cur.valid) set_tile();
+        // The L2 prefetch cursor runs kPrefetch k-blocks ahead of the loads.
+        // With the local layout its first burst is issued after the copies
+        // of the preloaded stages, before the dependency wait (measured: this
+        // order beat a burst after the wait and a burst from another thread).
+        if constexpr (!kLocal) {
+          for (int i = 0; i < kPrefetch; ++i) pf_step();
         }
-        cur.next(a, total_tiles, P, BN);
-      }
+        if constexpr (kLocal) {
+          int npre = 0;
+          int pre_kb[C::kStages], pre_m[C::kStages];
+          while (cur.valid && npre < C::kStages) {
+            arm();
+            load_w();
+            pre_kb[npre] = kb;
+            pre_m[npre] = cur.m_blk;
+            ++npre;
+            advance(false);   // these k-blocks are being loaded, not prefetched
+          }
+          for (int i = 0; i < kPrefetch; ++i) pf_step();
+          pdl_wait_prior();
+          if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
+          for (int i = 0; i < npre; ++i) load_x(i, pre_kb[i], pre_m[i]);
+        }
+        while (cur.valid && !abort_flag) {
+          bool ok;
+          { WS_T0(); ok = mbar_wait(&empty_bar[stage], phase ^ 1, a.status); WS_ADD(0); }
+          if (!ok) { abort_flag = 1; break; }
+          arm();
+          load_w();
+          load_x(stage, kb, cur.m_blk);
+          advance(true);
+        }
+        if constexpr (kLocal) {
+          // the layout derived from topk_ids must be the sort's
+          if (*a.num_padded != P && a.status) atomicOr(a.status, kDevBadExpert);
+        }
+      };
+      if (a.local)
+        produce(Seq16R{}, [&](const Seq16R& q) { return static_cast<int>(s_blk_expert[q.m_blk]); },
+                std::true_type{});
+      else
+        produce(Seq16{}, [](const Seq16& q) { return q.e; }, std::false_type{});
       // Copies still in flight into shared memory must land before the CTA
       // exits: normally every armed stage was consumed, so these return at
       // once; after an abort they wait (bounded) for the TMA.
@@ -278,16 +365,20 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
+    pdl_wait_prior();
+    const int P = a.local ? s_nblk * BN : *a.num_padded;
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      int slot = 0;
+      uint32_t slot_phase = 0;
       int local = 0;
 #ifdef MOE_TIMELINE
       int tl_mma = 1;
 #endif
       constexpr uint32_t idesc = idesc_dense(1, 1, kTileN, BN);
       const uint64_t b_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
-      Seq16 seq;
+      Seq16R seq;
       for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
@@ -300,14 +391,14 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         for (int kb = 0; kb < kblocks; ++kb) {
           bool ok1, ok2;
           { WS_T0(); ok1 = mbar_wait(&full_bar[stage], phase, a.status); WS_ADD(1); }
-          { WS_T0(); ok2 = ok1 && mbar_wait(&a_full[stage], phase, a.status); WS_ADD(2); }
+          { WS_T0(); ok2 = ok1 && mbar_wait(&a_full[slot], slot_phase, a.status); WS_ADD(2); }
           if (!ok2) { abort_flag = 1; break; }
 #ifdef MOE_TIMELINE
           if (tl_mma) { MOE_TL(3 + a.stage, 3); tl_mma = 0; }
 #endif
           tc_fence_after();
           const uint64_t bd = b_desc0 + static_cast<uint64_t>(stage) * (C::kStageBytes >> 4);
-          const uint32_t a_tmem = tmem + stage * kACols;
+          const uint32_t a_tmem = tmem + slot * kACols;
 #pragma unroll
           for (int kk = 0; kk < kTileK / kMmaK; ++kk) {
             // B: atom h of the stage, then 32 bytes (2 descriptor units) per MMA;
@@ -316,8 +407,9 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
             mma_f16_tmem_a(d_tmem, a_tmem + kk * (kMmaK / 2),
                            bd + h * (C::kBAtomBytes >> 4) + off, idesc, (kb | kk) != 0);
           }
-          tc_commit(&empty_bar[stage]);         // frees the smem stage and its TMEM slot
+          tc_commit(&empty_bar[stage]);         // frees the smem stage and the TMEM slot
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+          if (++slot == C::kASlots) { slot = 0; slot_phase ^= 1; }
         }
         tc_commit(&acc_full[ab]);
       }
@@ -327,6 +419,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     }
   } else if (warp >= 6) {
     // ---------------------------------------------------------- converters
+    pdl_wait_prior();
+    const int P = a.local ? s_nblk * BN : *a.num_padded;
     constexpr int kHalves = C::kConvWarps == 8 ? 1 : 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;                      // weight row = TMEM lane
@@ -337,7 +431,11 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     int stage = 0;
     uint32_t phase = 0;
-    Seq16 seq;
+    int slot = 0;                 // TMEM slot of this k-block
+    int lag_stage = 0;            // stage of k-block j - kASlots, whose MMA frees the slot
+    uint32_t lag_phase = 0;
+    int done = 0;                 // k-blocks converted so far
+    Seq16R seq;
     for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
       bool stop = false;
       for (int kb = 0; kb < kblocks; ++kb) {
@@ -350,7 +448,20 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           if (rep) WS_ADD(4);
 #endif
         }
-        okc2 = okc1;   // slot `stage` is free once the stage's data has landed
+        okc2 = okc1;
+        if constexpr (C::kStages > C::kASlots) {
+          // the slot is free once the MMA of k-block j - kASlots committed;
+          // with equal rings the landed stage implies it (the producer
+          // reloaded the stage only after that commit)
+          if (okc2 && done >= C::kASlots) {
+            WS_T0();
+            okc2 = mbar_wait(&empty_bar[lag_stage], lag_phase, a.status);
+#ifdef MOE_WAIT_STATS
+            if (rep) WS_ADD(5);
+#endif
+            if (++lag_stage == C::kStages) { lag_stage = 0; lag_phase ^= 1; }
+          }
+        }
 #ifdef MOE_WAIT_STATS
         const long long _cb0 = clock64();
 #endif
@@ -379,29 +490,33 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
                 out[cc * 16 + wi * 4 + b] = bf16x2_mul(lut_lane[idx * 32], sc);
               }
           }
-          tmem_st_32x32b_x32(t_row + stage * kACols + h * 32, out);
+          tmem_st_32x32b_x32(t_row + slot * kACols + h * 32, out);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[stage]);
+        if (lane == 0) mbar_arrive(&a_full[slot]);
 #ifdef MOE_WAIT_STATS
         if (rep)
           atomicAdd(reinterpret_cast<unsigned long long*>(&g_ws16[blockIdx.x & 511][a.stage - 1][6]),
                     static_cast<unsigned long long>(clock64() - _cb0));
 #endif
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        if (++slot == C::kASlots) slot = 0;
+        ++done;
       }
       if (stop) break;
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait_prior();
+    const int P = a.local ? s_nblk * BN : *a.num_padded;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int et = threadIdx.x - 64;
     const int R = a.M * a.topk;
     int local = 0;
-    Seq16 seq;
+    Seq16R seq;
     for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
       const int m_blk = seq.m_blk, n_tile = seq.n_tile;
       const int ab = local % C::kAccBufs;
@@ -608,6 +723,9 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.n_tiles = a.N / kTileN;
   a.num_blocks = static_cast<int>(g.p_max / g.bm);
   a.n_group_log2 = stage == 1 ? 0 : stage2_n_group_log2(g.M, g.p_max * g.Ip * 2, a.n_tiles);
+  a.local = static_cast<int64_t>(g.M) * g.topk <= kLocalMaxRoutes &&
+            a.num_blocks <= kLocalMaxBlocks ? 1 : 0;
+  a.topk_ids = g.topk_ids;
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
   a.num_padded = g.num_padded;
   a.sfa = stage == 1 ? g.w1s : g.w2s;

@@ -70,6 +70,8 @@ struct MxArgs {
   int n_tiles;           // N / 128
   int num_blocks;        // p_max / block_m
   int n_group_log2;      // stage 2: log2 of the feature tiles per walk group
+  int local;             // derive the route layout from topk_ids (decode sizes)
+  const int32_t* topk_ids;
   const int32_t* sorted_route;
   const float* sorted_w;
   const int32_t* block_expert;
@@ -112,14 +114,16 @@ struct Cfg {
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64
                                    : kColsNeeded <= 128 ? 128 : kColsNeeded <= 256 ? 256 : 512;
   static constexpr int kEpiFloats = 32 * (64 + 4);             // stage-1 / stage-2 transpose tile
-  static constexpr int kRouteBytes = 256 * 8;                  // per-tile route info
+  static constexpr int kRouteBytes = BN * 8;                   // per-tile route info
   static constexpr int kSmem =
       1024 /*align slack*/ + kStages * kStageBytes + kEpiFloats * 4 + kRouteBytes + 256;
   // TMA transaction bytes of one stage: FP4 A counts packed bytes
   static constexpr uint32_t kTxBytes = kTileN * kTileK / 2 + kBBytes + kSfBytes;
   static_assert(kColsNeeded <= 512 / kCtasPerSm, "TMEM budget");
   // per SM: 228 KB of shared memory, of which 1 KB is reserved per CTA
-  static_assert(kCtasPerSm * (kSmem + 2048) <= 228 * 1024, "smem budget");
+  // per SM: 228 KB, of which 1 KB is reserved per CTA; the static shared
+  // variables (barriers, the local route layout) take up to kStaticSmem
+  static_assert(kCtasPerSm * (kSmem + 1024 + kStaticSmem) <= 228 * 1024, "smem budget");
 };
 
 
@@ -129,7 +133,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
                        const __grid_constant__ CUtensorMap tmB, const MxArgs a) {
   using C = Cfg<BN>;
   // SPLIT: stage 1 with the tail split (SplitSeq units, partial-sum epilogue)
+  // the producer's walk loads each tile's expert; the other roles' walks do not
   using Seq = typename std::conditional<SPLIT, SplitSeq<MxArgs>, TileSeq<MxArgs>>::type;
+  using SeqR = typename std::conditional<SPLIT, SplitSeq<MxArgs, false>,
+                                         TileSeq<MxArgs, false>>::type;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic so that the
   // compiler keeps every access below in the shared state space
@@ -137,13 +144,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
   uint8_t* stages = smem;
   float* epi = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token (stage 2) / -1 pad
-  float* s_w = reinterpret_cast<float*>(s_tok + 256);             // [BN] routing weight
+  float* s_w = reinterpret_cast<float*>(s_tok + BN);              // [BN] routing weight
   __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
   __shared__ uint64_t acc_full[C::kAccBufs], acc_empty[C::kAccBufs];
   __shared__ uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ int split_last;
+  __shared__ uint16_t s_blk_expert[kLocalMaxBlocks];   // local layout: expert of each route block
+  __shared__ int s_nblk;                               // local layout: number of route blocks
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();
@@ -173,14 +182,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     tmem_alloc(&tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  // Decode sizes: the route layout (route blocks per expert) is derived here
+  // from topk_ids, an input of the call that is complete before the call's
+  // first kernel starts, so the producer can load its first weight tiles
+  // before the previous kernel has finished (see LocalLayout).
+  if (a.local) {
+    // the epilogue's transpose buffer is free until the first tile's epilogue
+    const int nb = local_block_layout(a.topk_ids, a.M * a.topk, a.E, BN,
+                                      reinterpret_cast<int*>(epi), s_blk_expert);
+    if (threadIdx.x == 0) s_nblk = nb;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  // everything above overlaps the previous kernel; its outputs are read below
-  pdl_wait_prior();
-  if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
-  const int P = *a.num_padded;
   const uint32_t sf_col0 = C::kAccBufs * C::kAccCols;
 
   if (warp == 0) {
@@ -189,7 +204,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     // consecutive 8 KB blocks), both scale arrays and the route rows advance
     // by constant steps. A second cursor runs kPrefetch k-blocks ahead
     // (across tiles) and prefetches weight tiles into L2, so the loads that
-    // fill the shared-memory ring mostly hit L2.
+    // fill the shared-memory ring mostly hit L2. With the local layout the
+    // weight half of the first ring stages (weights and their scales) is
+    // loaded before the dependency wait and the route half after it.
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_x = policy_evict_last();    // routes: reused across n-tiles
@@ -201,54 +218,56 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       uint32_t phase = 0;
       uint32_t armed_mask = 0, armed_par = 0;   // stages armed, parity of their last arming
       uint8_t* sbase = stages;
-      Seq cur;
-      seq_init(cur, a, total_tiles, P, BN, kblocks);
 #ifdef MOE_TIMELINE
       int tl_first = 1;
 #endif
-      Seq pf = cur;
-      int pf_kb = 0;
-      const uint8_t* pf_w = nullptr;
-      auto pf_tile = [&]() {
-        pf_w = a.w_base + (static_cast<int64_t>(pf.e) * a.n_tiles + pf.n_tile) * kblocks * kWTile;
-        pf_kb = seq_kb0(pf);
-      };
-      if (pf.valid) pf_tile();
-      auto pf_step = [&]() {
-        if (!pf.valid) return;
-        bulk_prefetch_l2(pf_w + static_cast<int64_t>(pf_kb) * kWTile, kWTile);
-        if (++pf_kb == seq_kb1(pf, kblocks)) {
-          seq_next(pf, a, total_tiles, P, BN);
-          if (pf.valid) pf_tile();
+      auto produce = [&](auto cur, auto expert_of, auto local_mode) {
+        constexpr bool kLocal = decltype(local_mode)::value;
+        int P;
+        if constexpr (kLocal) {
+          P = s_nblk * BN;
+        } else {
+          pdl_wait_prior();
+          if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
+          P = *a.num_padded;
         }
-      };
-      for (int i = 0; i < kPrefetch; ++i) pf_step();
-      while (cur.valid && !abort_flag) {
-        const int64_t wtile = static_cast<int64_t>(cur.e) * a.n_tiles + cur.n_tile;
-        const int kb_begin = seq_kb0(cur), kb_end = seq_kb1(cur, kblocks);
-        int row_a = static_cast<int>((wtile * kblocks + kb_begin) * kTileN);
-        const uint8_t* sfa = a.sfa + (wtile * kblocks + kb_begin) * 512;
-        const uint8_t* sfb =
-            a.sfb + (static_cast<int64_t>(cur.m_blk) * kblocks + kb_begin) * C::kNa * 512;
-        const int row_b = cur.m_blk * BN;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
-          {
-            WAIT_T0();
-            if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
-            WAIT_ADD(0);
+        seq_init(cur, a, total_tiles, P, BN, kblocks);
+        auto pf = cur;
+        int pf_kb = 0;
+        const uint8_t* pf_w = nullptr;
+        auto pf_tile = [&]() {
+          pf_w = a.w_base + (static_cast<int64_t>(expert_of(pf)) * a.n_tiles + pf.n_tile) *
+                                kblocks * kWTile;
+          pf_kb = seq_kb0(pf);
+        };
+        if (pf.valid) pf_tile();
+        auto pf_skip = [&]() {
+          if (++pf_kb == seq_kb1(pf, kblocks)) {
+            seq_next(pf, a, total_tiles, P, BN);
+            if (pf.valid) pf_tile();
           }
-          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
-          armed_mask |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-#ifdef MOE_TIMELINE
-          if (tl_first) { MOE_TL(3 + a.stage, 2); tl_first = 0; }
-#endif
-          tma_load_2d(sbase, &tmA, &full_bar[stage], 0, row_a, pol_w);
-          tma_load_2d(sbase + C::kABytes, &tmB, &full_bar[stage], kb * kTileK, row_b, pol_x);
-          bulk_load(sbase + C::kABytes + C::kBBytes, sfa, 512, &full_bar[stage], pol_w);
-          bulk_load(sbase + C::kABytes + C::kBBytes + 512, sfb, 512 * C::kNa, &full_bar[stage],
-                    pol_x);
-          pf_step();
+        };
+        auto pf_step = [&]() {
+          if (!pf.valid) return;
+          bulk_prefetch_l2(pf_w + static_cast<int64_t>(pf_kb) * kWTile, kWTile);
+          pf_skip();
+        };
+        // flat walk over the k-blocks of this CTA's tiles
+        int kb = 0, kb_end = 0, row_a = 0, row_b = 0;
+        const uint8_t* sfa = nullptr;
+        const uint8_t* sfb = nullptr;
+        auto set_tile = [&]() {
+          const int64_t wtile = static_cast<int64_t>(expert_of(cur)) * a.n_tiles + cur.n_tile;
+          kb = seq_kb0(cur);
+          kb_end = seq_kb1(cur, kblocks);
+          row_a = static_cast<int>((wtile * kblocks + kb) * kTileN);
+          sfa = a.sfa + (wtile * kblocks + kb) * 512;
+          sfb = a.sfb + (static_cast<int64_t>(cur.m_blk) * kblocks + kb) * C::kNa * 512;
+          row_b = cur.m_blk * BN;
+        };
+        auto advance = [&](bool prefetch) {
+          if (prefetch) pf_step();
+          else if (pf.valid) pf_skip();
           row_a += kTileN;
           sfa += 512;
           sfb += 512 * C::kNa;
@@ -259,9 +278,76 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
           } else {
             sbase += C::kStageBytes;
           }
+          if (++kb == kb_end) {
+            seq_next(cur, a, total_tiles, P, BN);
+            if (cur.valid) set_tile();
+          }
+        };
+        auto arm = [&]() {
+          mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
+          armed_mask |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+#ifdef MOE_TIMELINE
+          if (tl_first) { MOE_TL(3 + a.stage, 2); tl_first = 0; }
+#endif
+        };
+        auto load_w = [&]() {
+          tma_load_2d(sbase, &tmA, &full_bar[stage], 0, row_a, pol_w);
+          bulk_load(sbase + C::kABytes + C::kBBytes, sfa, 512, &full_bar[stage], pol_w);
+        };
+        auto load_x = [&](uint8_t* sb, uint64_t* bar, int kbx, int rb, const uint8_t* sfbx) {
+          tma_load_2d(sb + C::kABytes, &tmB, bar, kbx * kTileK, rb, pol_x);
+          bulk_load(sb + C::kABytes + C::kBBytes + 512, sfbx, 512 * C::kNa, bar, pol_x);
+        };
+        if (cur.valid) set_tile();
+        // The L2 prefetch cursor runs kPrefetch k-blocks ahead of the loads.
+        // With the local layout its first burst is issued after the copies
+        // of the preloaded stages, before the dependency wait (measured: this
+        // order beat a burst after the wait and a burst from another thread).
+        if constexpr (!kLocal) {
+          for (int i = 0; i < kPrefetch; ++i) pf_step();
         }
-        seq_next(cur, a, total_tiles, P, BN);
-      }
+        if constexpr (kLocal) {
+          // the first ring stages: weights now, routes after the wait
+          int npre = 0;
+          int pre_kb[C::kStages], pre_rb[C::kStages];
+          const uint8_t* pre_sfb[C::kStages];
+          while (cur.valid && npre < C::kStages) {
+            arm();
+            load_w();
+            pre_kb[npre] = kb;
+            pre_rb[npre] = row_b;
+            pre_sfb[npre] = sfb;
+            ++npre;
+            advance(false);   // these k-blocks are being loaded, not prefetched
+          }
+          for (int i = 0; i < kPrefetch; ++i) pf_step();
+          pdl_wait_prior();
+          if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
+          for (int i = 0; i < npre; ++i)
+            load_x(stages + i * C::kStageBytes, &full_bar[i], pre_kb[i], pre_rb[i], pre_sfb[i]);
+        }
+        while (cur.valid && !abort_flag) {
+          {
+            WAIT_T0();
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1, a.status)) { abort_flag = 1; break; }
+            WAIT_ADD(0);
+          }
+          arm();
+          load_w();
+          load_x(sbase, &full_bar[stage], kb, row_b, sfb);
+          advance(true);
+        }
+        if constexpr (kLocal) {
+          // the layout derived from topk_ids must be the sort's
+          if (*a.num_padded != P && a.status) atomicOr(a.status, kDevBadExpert);
+        }
+      };
+      if (a.local)
+        produce(SeqR{}, [&](const SeqR& q) { return static_cast<int>(s_blk_expert[q.m_blk]); },
+                std::true_type{});
+      else
+        produce(Seq{}, [](const Seq& q) { return q.e; }, std::false_type{});
       // Copies still in flight into shared memory must land before the CTA
       // exits: normally the MMA thread consumed every armed stage, so these
       // return at once; after an abort they wait (bounded) for the TMA.
@@ -274,6 +360,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     // this loop is kept minimal: descriptors are built once and advanced by
     // adding to their 14-bit start-address field (address >> 4), instruction
     // descriptors are compile-time constants.
+    pdl_wait_prior();
+    const int P = a.local ? s_nblk * BN : *a.num_padded;
     if (lane == 0) {
       const uint64_t a_desc0 = smem_desc(smem_u32(stages), 16, 1024, kSwizzle128B);
       const uint64_t b_desc0 = smem_desc(smem_u32(stages + C::kABytes), 16, 1024, kSwizzle128B);
@@ -285,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       uint32_t sdesc_off = 0;                                // stage * kStageStep
       uint32_t sf_tmem = tmem + sf_col0;                      // this stage's scale columns
       int local = 0;
-      Seq seq;
+      SeqR seq;
 #ifdef MOE_TIMELINE
       int tl_mma = 1;
 #endif
@@ -343,12 +431,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait_prior();
+    const int P = a.local ? s_nblk * BN : *a.num_padded;
     const int quad = warp & 3;               // TMEM lane quadrant
     const int row = quad * 32 + lane;        // weight row within the tile
     const int et = threadIdx.x - 64;         // 0..127
     const int R = a.M * a.topk;
     int local = 0;
-    Seq seq;
+    SeqR seq;
     for (seq_init(seq, a, total_tiles, P, BN, kblocks); seq.valid;
          seq_next(seq, a, total_tiles, P, BN)) {
       const int m_blk = seq.m_blk, n_tile = seq.n_tile;
@@ -676,6 +766,9 @@ cudaError_t prepare_gemm_mx(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.n_tiles = a.N / kTileN;
   a.num_blocks = static_cast<int>(g.p_max / g.bm);
   a.n_group_log2 = stage == 1 ? 0 : stage2_n_group_log2(g.M, g.p_max * g.Ip * 1, a.n_tiles);
+  a.local = static_cast<int64_t>(g.M) * g.topk <= kLocalMaxRoutes &&
+            a.num_blocks <= kLocalMaxBlocks ? 1 : 0;
+  a.topk_ids = g.topk_ids;
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
   a.num_padded = g.num_padded;
   a.sfa = stage == 1 ? g.w1s : g.w2s;

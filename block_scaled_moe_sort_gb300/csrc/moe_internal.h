@@ -52,6 +52,7 @@ struct GemmArgs {
   bool a16;
   int M, H, Ip, E, topk, bm;
   int64_t p_max;
+  const int32_t* topk_ids;   // the call's routing input (local layout at decode sizes)
   const int32_t* sorted_route;
   const float* sorted_w;
   const int32_t* block_expert;

@@ -195,6 +195,7 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   g.a16 = a16;
   g.M = M; g.H = H; g.Ip = Ip; g.E = E; g.topk = topk; g.bm = L.block_m;
   g.p_max = L.p_max;
+  g.topk_ids = ids;
   g.sorted_route = sorted_route; g.sorted_w = sorted_w; g.block_expert = block_expert;
   g.num_padded = num_padded;
   g.w1 = w1; g.w1s = w1s; g.w2 = w2; g.w2s = w2s;
