@@ -255,8 +255,8 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
  * inside this library; each GPU that loads the library keeps it until the
  * process exits. Shapes whose fused_moe_workspace_bytes() exceeds that size
  * are rejected with MOE_ERR_WORKSPACE before anything is launched (with the
- * current workspace layout that is up to 23 tokens at H=5120, Ip=640, 384
- * experts, top-6, and up to 69 tokens at 128 experts, top-3).
+ * current workspace layout that is up to 19 tokens at H=5120, Ip=640, 384
+ * experts, top-6, and up to 38 tokens at 128 experts, top-3).
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any
