@@ -7,9 +7,11 @@ at the largest decode bucket of its sweep, M=768 tokens, H=5120,
 I=576 padded to 640, 384 experts, top-6, uniform routing, seeded synthetic
 inputs (AITER #5609 "Add DeepSeek V4.1 Flash TP4 gfx950 MoE tuning",
 Configuration). The other buckets of that sweep are reported under "sweep",
-and the gating kernel (router logits -> top-k ids and weights, 384 experts,
+the gating kernel (router logits -> top-k ids and weights, 384 experts,
 top-6) at the bench M and at M=16384 under "router" (µs, GB/s of logits
-read and ids/weights written, fraction of measured HBM).
+read and ids/weights written, fraction of measured HBM), and the gated call
+(router logits in, gating inside the call) at M=6 and the bench M under
+"gated".
 
 The prefill half of the metric is reported under "prefill": the skewed
 prefill stress (backbone a8w4, M=16384, Zipf(1.2) routing) and the a16w4
@@ -527,6 +529,45 @@ def main():
                                    "gbs": round(nbytes / us / 1e3, 1),
                                    "hbm_frac": round(nbytes / us / 1e3 / hbm, 3)}
 
+    # ---- gated calls (router logits -> gating + fused call), at decode
+    # sizes with the gating inside the call's first kernel and at the bench M
+    gated = {}
+    if not args.no_sweep and not shape.a16:
+        e_s = torch.cuda.Event(enable_timing=True)
+        e_e = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for Mg in sorted({6, M}):
+                gr = torch.Generator().manual_seed(6000 + Mg)
+                lg = torch.randn(Mg, shape.E_route, generator=gr, dtype=torch.float32).to(dev)
+                xg = mi.make_case(geo, Mg, routing=routing, weights=weights).x.to(dev)
+                og = torch.empty(Mg, shape.H, dtype=torch.bfloat16, device=dev)
+                ig = torch.empty(Mg, k, dtype=torch.int32, device=dev)
+                wg = torch.empty(Mg, k, dtype=torch.float32, device=dev)
+                wsg = torch.empty(layer.workspace_bytes(Mg, k), dtype=torch.uint8, device=dev)
+
+                def gcall():
+                    m.fused_moe_gated(xg, lg, k, layer.w1, layer.w1_scale, layer.w2,
+                                      layer.w2_scale, layer.E, layer.Ip, out=og, ws=wsg,
+                                      topk_ids=ig, topk_weights=wg, stream=stream)
+                for _ in range(3):
+                    gcall()
+                torch.cuda.synchronize()
+                gg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gg, stream=stream):
+                    gcall()
+                ts = []
+                for _ in range(10):
+                    flush.zero_()
+                    e_s.record(stream)
+                    gg.replay()
+                    e_e.record(stream)
+                    e_e.synchronize()
+                    ts.append(e_s.elapsed_time(e_e))
+                gated[str(Mg)] = {"us": round(statistics.median(ts) * 1000, 2),
+                                  "front": "one launch (gating, sort, gather)" if Mg * k <= 256
+                                  else "gating launch + sort + gather"}
+                del gg
+
     prefill = {}
     if not args.no_prefill:
         with torch.cuda.stream(stream):
@@ -567,6 +608,8 @@ def main():
         line["router"] = router
     if prefill:
         line["prefill"] = prefill
+    if gated:
+        line["gated"] = gated
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, shape)
     if rank == 0:

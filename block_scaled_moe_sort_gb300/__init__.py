@@ -22,7 +22,7 @@ __all__ = [
     "moe_prepack_scales_mx", "moe_prepack_weights_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
     "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS", "fused_moe_a8w4_noalloc",
-    "moe_noalloc_status",
+    "moe_noalloc_status", "fused_moe_gated",
 ]
 
 HEADER = os.path.join(_build.ROOT, "include", "moe_mx.h")
@@ -82,6 +82,14 @@ _SIGS = {
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
                                         _c_int, _c_void_p, _c_void_p]),
     "moe_noalloc_status": (_c_int, [_c_void_p, _c_void_p]),
+    "fused_moe_a8w4_gated": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                      _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
+                                      _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                      _c_size_t, _c_void_p]),
+    "fused_moe_a16w4_gated": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                       _c_int, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                       _c_size_t, _c_void_p]),
     "moe_profile_enable": (_c_int, [_c_int]),
     "moe_profile_collect": (_c_int, [ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_int32)]),
@@ -318,6 +326,36 @@ def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_pa
                   w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m)
 
 
+def fused_moe_gated(x, router_logits, topk, w1_packed, w1_scale_packed, w2_packed,
+                    w2_scale_packed, E, Ip, a16=False, shared_id=None, out=None, ws=None,
+                    topk_ids=None, topk_weights=None, stream=None):
+    """The fused call with the gating in front: router logits float32
+    [M, E_route] -> (out BF16 [M, H], topk_ids int32 [M, k'], topk_weights
+    float32 [M, k']), k' = topk (+1 with a shared expert)."""
+    M, H = x.shape
+    assert router_logits.dtype == torch.float32 and router_logits.stride(1) == 1
+    E_route = router_logits.shape[1]
+    kout = topk + (1 if shared_id is not None else 0)
+    dev = x.device
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty(M, kout, dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty(M, kout, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(max(fused_moe_workspace_bytes(M, H, Ip, E, kout, a16), 1),
+                         dtype=torch.uint8, device=dev)
+    fn = "fused_moe_a16w4_gated" if a16 else "fused_moe_a8w4_gated"
+    code = getattr(lib(), fn)(
+        _ptr(x), _ptr(router_logits), router_logits.stride(0), E_route, topk,
+        -1 if shared_id is None else shared_id, M, H, _ptr(w1_packed), _ptr(w1_scale_packed),
+        _ptr(w2_packed), _ptr(w2_scale_packed), E, Ip, _ptr(out), _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(ws), ws.numel(), _stream(stream))
+    _check(fn, code)
+    return out, topk_ids, topk_weights
+
+
 NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -436,6 +474,16 @@ class MoeLayer:
         this layer, with the shared expert's column when it has one."""
         assert logits.shape[1] == self.E_routed
         return moe_router_topk(logits, topk, shared_id=self.shared_id, stream=stream)
+
+    def forward_gated(self, x, router_logits, topk: int, out=None, ws=None, stream=None):
+        """Gating + fused call in one (fused_moe_*_gated): router logits
+        float32 [M, E_route] -> (out, topk_ids, topk_weights); the shared
+        expert's column is added when the layer has one. An expert-parallel
+        shard passes the global logits (ids outside its experts are
+        dropped)."""
+        return fused_moe_gated(x, router_logits, topk, self.w1, self.w1_scale, self.w2,
+                               self.w2_scale, self.E, self.Ip, a16=self.a16,
+                               shared_id=self.shared_id, out=out, ws=ws, stream=stream)
 
     def block_m_for(self, M: int, topk: Optional[int] = None) -> int:
         """Route block for an M-token call (0 = the library's rule)."""

@@ -723,7 +723,7 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.n_tiles = a.N / kTileN;
   a.num_blocks = static_cast<int>(g.p_max / g.bm);
   a.n_group_log2 = stage == 1 ? 0 : stage2_n_group_log2(g.M, g.p_max * g.Ip * 2, a.n_tiles);
-  a.local = static_cast<int64_t>(g.M) * g.topk <= kLocalMaxRoutes &&
+  a.local = g.topk_ids && static_cast<int64_t>(g.M) * g.topk <= kLocalMaxRoutes &&
             a.num_blocks <= kLocalMaxBlocks ? 1 : 0;
   a.topk_ids = g.topk_ids;
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;

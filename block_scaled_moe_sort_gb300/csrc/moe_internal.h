@@ -30,14 +30,27 @@ cudaError_t launch_prepack_weights(const uint8_t* w, int E, int N, int K, uint8_
 cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uint8_t* out,
                                   cudaStream_t s);
 
+// Gating inside the decode front kernel (the gated calls): router logits
+// [M, ld] of E_route experts; topk_sel picks per token plus, with
+// shared_id >= 0, the shared expert column; the ids and weights are written
+// to ids_out / w_out [M, topk] as well.
+struct FrontGating {
+  const float* logits;
+  int ld, E_route, topk_sel, shared_id;
+  int32_t* ids_out;
+  float* w_out;
+};
+
 // Few routes (M * topk <= kFrontMaxRoutes): the sort and the gather in one
-// launch; writes everything launch_sort and launch_gather_act write.
+// launch; writes everything launch_sort and launch_gather_act write. With
+// gate, the routes come from the router logits instead of ids / wts.
 cudaError_t launch_front_tiny(bool a16, const void* x, const int32_t* ids, const float* wts, int M,
                               int H, int topk, int E, int bm, int64_t p_max,
                               int32_t* sorted_route, float* sorted_w, int32_t* block_expert,
                               int32_t* expert_off, int32_t* num_padded, int32_t* route_pos,
                               int32_t* status, void* act, uint8_t* act_sf, float* acc,
-                              void* zero2, int64_t zero2_bytes, cudaStream_t s);
+                              void* zero2, int64_t zero2_bytes, const FrontGating* gate,
+                              cudaStream_t s);
 
 // Writes each token's activation row to the sorted position of each of its
 // routes (quantised to FP8 with scale atoms for a8w4, as BF16 for a16w4) and

@@ -130,10 +130,13 @@ void prof_end_call() {
   else ++g_prof.dropped;
 }
 
+// gate: the gated calls (routing from router logits, written to gate->ids_out /
+// w_out, which then stand for ids / wts); nullptr for the plain calls.
 moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const float* wts, int M,
                             int H, int topk, const uint8_t* w1, const uint8_t* w1s,
                             const uint8_t* w2, const uint8_t* w2s, int E, int Ip, void* out,
-                            void* ws, size_t ws_bytes, int bm_req, cudaStream_t s) {
+                            void* ws, size_t ws_bytes, int bm_req, cudaStream_t s,
+                            const FrontGating* gate = nullptr) {
   moe_status_t st = check_shape(M, H, Ip, E, topk);
   if (st != MOE_OK) return st;
   if (bm_req != 0 && !valid_bm(bm_req)) return MOE_ERR_UNSUPPORTED;
@@ -169,17 +172,23 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
 
   cudaError_t e;
   if (R <= kFrontMaxRoutes) {
-    // decode: sort and gather in one launch (profiled as the sort slot)
+    // decode: gating (gated calls), sort and gather in one launch (profiled
+    // as the sort slot)
     prof_mark(0, true, s);
     e = launch_front_tiny(a16, x, ids, wts, M, H, topk, E, L.block_m, L.p_max, sorted_route,
                           sorted_w, block_expert, expert_off, num_padded, route_pos, status, act,
-                          act_sf, acc, split_part, split_bytes, s);
+                          act_sf, acc, split_part, split_bytes, gate, s);
     if (e != cudaSuccess) return from_cuda(e);
     prof_mark(0, false, s);
     prof_mark(1, true, s);
     prof_mark(1, false, s);
   } else {
     prof_mark(0, true, s);
+    if (gate) {
+      e = launch_router_topk(gate->logits, M, gate->E_route, gate->ld, gate->topk_sel,
+                             gate->shared_id, gate->ids_out, gate->w_out, s);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
     int32_t* sort_scratch = reinterpret_cast<int32_t*>(base + L.sort_scratch_off);
     e = launch_sort(ids, wts, R, E, L.block_m, L.p_max, sorted_route, sorted_w, block_expert,
                     expert_off, num_padded, route_pos, status, sort_scratch, s);
@@ -195,7 +204,9 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   g.a16 = a16;
   g.M = M; g.H = H; g.Ip = Ip; g.E = E; g.topk = topk; g.bm = L.block_m;
   g.p_max = L.p_max;
-  g.topk_ids = ids;
+  // the GEMMs may read topk_ids before their dependency wait only when it is
+  // an input of the call (not when the gating kernel writes it)
+  g.topk_ids = gate ? nullptr : ids;
   g.sorted_route = sorted_route; g.sorted_w = sorted_w; g.block_expert = block_expert;
   g.num_padded = num_padded;
   g.w1 = w1; g.w1s = w1s; g.w2 = w2; g.w2s = w2s;
@@ -386,6 +397,49 @@ moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids, const float
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   return fused_moe_a16w4_bm(x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale, E,
                             Ip, out, ws, ws_bytes, 0, stream);
+}
+
+namespace {
+moe_status_t gated_call(bool a16, const void* x, const float* logits, int ld, int E_route,
+                        int topk, int shared_id, int M, int H, const uint8_t* w1,
+                        const uint8_t* w1_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                        int E, int Ip, void* out, int32_t* topk_ids, float* topk_weights,
+                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (M < 0 || E_route <= 0 || ld < E_route || topk < 1 || topk > E_route)
+    return MOE_ERR_INVALID_ARG;
+  if (shared_id >= 0 && (shared_id < E_route || shared_id >= kMaxExperts))
+    return MOE_ERR_INVALID_ARG;
+  if (E_route > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  const int kout = topk + (shared_id >= 0 ? 1 : 0);
+  if (kout > kMaxTopk) return MOE_ERR_UNSUPPORTED;
+  if (M > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+  if (M > 0 && (!aligned(logits) || !aligned(topk_ids) || !aligned(topk_weights)))
+    return MOE_ERR_ALIGNMENT;
+  FrontGating gate{logits, ld, E_route, topk, shared_id, topk_ids, topk_weights};
+  return fused_moe_impl(a16, x, topk_ids, topk_weights, M, H, kout, w1, w1_scale, w2, w2_scale,
+                        E, Ip, out, ws, ws_bytes, 0, reinterpret_cast<cudaStream_t>(stream),
+                        &gate);
+}
+}  // namespace
+
+moe_status_t fused_moe_a8w4_gated(const void* x, const float* router_logits, int ld, int E_route,
+                                  int topk, int shared_id, int M, int H, const uint8_t* w1,
+                                  const uint8_t* w1_scale, const uint8_t* w2,
+                                  const uint8_t* w2_scale, int E, int Ip, void* out,
+                                  int32_t* topk_ids, float* topk_weights, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+  return gated_call(false, x, router_logits, ld, E_route, topk, shared_id, M, H, w1, w1_scale, w2,
+                    w2_scale, E, Ip, out, topk_ids, topk_weights, ws, ws_bytes, stream);
+}
+
+moe_status_t fused_moe_a16w4_gated(const void* x, const float* router_logits, int ld,
+                                   int E_route, int topk, int shared_id, int M, int H,
+                                   const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
+                                   const uint8_t* w2_scale, int E, int Ip, void* out,
+                                   int32_t* topk_ids, float* topk_weights, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  return gated_call(true, x, router_logits, ld, E_route, topk, shared_id, M, H, w1, w1_scale, w2,
+                    w2_scale, E, Ip, out, topk_ids, topk_weights, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_profile_enable(int enable) {

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include "common.cuh"
 #include "moe_internal.h"
+#include "router_warp.cuh"
 #include "sm100_ptx.cuh"
 #include "timeline.cuh"
 
@@ -177,12 +178,21 @@ struct FrontArgs {
   float* acc;
   float4* zero2;
   int64_t zero2_n4;
+  // gated call: routing from router logits [M, ld] of E_route experts
+  // (topk picks plus an optional shared expert column, a.topk columns in all)
+  const float* logits;
+  int ld, E_route, topk_sel, shared_id;
+  int32_t* ids_out;     // [M, topk] written by CTA 0
+  float* w_out;
 };
 
-template <bool A16>
+// SLOTS > 0: the gated call; every CTA selects every token's experts from
+// the router logits (one warp per token) before it sorts.
+template <bool A16, int SLOTS>
 __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
   __shared__ int e_s[kFrontMaxRoutes];     // expert of route r, -1 when dropped
   __shared__ int pos_s[kFrontMaxRoutes];   // sorted position of route r, -1 when dropped
+  __shared__ float w_s[SLOTS > 0 ? kFrontMaxRoutes : 1];   // gated: routing weight of route r
   __shared__ int cnt[kMaxExperts];
   __shared__ int off[kMaxExperts + 1];     // padded segment starts; off[E] = P
   const int tid = threadIdx.x, lane = tid & 31;
@@ -203,9 +213,29 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
     for (int q = 0; q < 4; ++q) raw[q] = __ldg(src + q);
   }
   for (int i = tid; i < a.E; i += blockDim.x) cnt[i] = 0;
+  if constexpr (SLOTS > 0) {
+    // gating: warp w selects tokens w, w + 8, ...; the raw ids go to e_s
+    for (int tt = tid >> 5; tt < a.M; tt += blockDim.x >> 5) {
+      uint32_t v[SLOTS];
+      router_load<SLOTS>(a.logits + static_cast<int64_t>(tt) * a.ld, a.E_route, lane, v);
+      int e;
+      float w;
+      router_select<SLOTS>(v, a.topk_sel, lane, &e, &w);
+      if (lane == a.topk_sel && a.shared_id >= 0) { e = a.shared_id; w = 1.f; }
+      if (lane < a.topk) {
+        const int r = tt * a.topk + lane;
+        e_s[r] = e;
+        w_s[r] = w;
+        if (blockIdx.x == 0) {
+          a.ids_out[r] = e;
+          a.w_out[r] = w;
+        }
+      }
+    }
+  }
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) {
-    const int v = __ldg(a.ids + r);
+    const int v = SLOTS > 0 ? e_s[r] : __ldg(a.ids + r);
     const int e = v >= 0 && v < a.E ? v : -1;
     e_s[r] = e;
     if (e >= 0) atomicAdd(&cnt[e], 1);
@@ -248,7 +278,7 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
       a.route_pos[r] = p;
       if (p >= 0) {
         a.sorted_route[p] = r;
-        a.sorted_w[p] = __ldg(a.wts + r);
+        a.sorted_w[p] = SLOTS > 0 ? w_s[r] : __ldg(a.wts + r);
       }
     }
     for (int e = tid; e < a.E; e += blockDim.x) {
@@ -434,12 +464,23 @@ cudaError_t launch_front_tiny(bool a16, const void* x, const int32_t* ids, const
                               int32_t* sorted_route, float* sorted_w, int32_t* block_expert,
                               int32_t* expert_off, int32_t* num_padded, int32_t* route_pos,
                               int32_t* status, void* act, uint8_t* act_sf, float* acc,
-                              void* zero2, int64_t zero2_bytes, cudaStream_t s) {
+                              void* zero2, int64_t zero2_bytes, const FrontGating* gate,
+                              cudaStream_t s) {
   const int R = M * topk;
   if (R > kFrontMaxRoutes || topk > 32 || E > kMaxExperts) return cudaErrorInvalidValue;
   FrontArgs a{ids, wts, static_cast<const __nv_bfloat16*>(x), M, H, topk, E, bm, p_max,
               sorted_route, sorted_w, block_expert, expert_off, num_padded, route_pos, status,
-              act, act_sf, acc, static_cast<float4*>(zero2), zero2 ? zero2_bytes / 16 : 0};
+              act, act_sf, acc, static_cast<float4*>(zero2), zero2 ? zero2_bytes / 16 : 0,
+              nullptr, 0, 0, 0, -1, nullptr, nullptr};
+  if (gate) {
+    a.logits = gate->logits;
+    a.ld = gate->ld;
+    a.E_route = gate->E_route;
+    a.topk_sel = gate->topk_sel;
+    a.shared_id = gate->shared_id;
+    a.ids_out = gate->ids_out;
+    a.w_out = gate->w_out;
+  }
   const int64_t warps = static_cast<int64_t>(M) * ((H / 32 + 31) / 32);
   const int64_t zero_bytes = zero2_bytes;
   int64_t g = (warps + 7) / 8;
@@ -447,8 +488,15 @@ cudaError_t launch_front_tiny(bool a16, const void* x, const int32_t* ids, const
   if (gz > g) g = gz < 152 * 8 ? gz : 152 * 8;
   const int grid = g > 0 ? static_cast<int>(g) : 1;
   // first kernel of the call: an ordinary launch (ordered after all earlier work)
-  if (a16) front_tiny_kernel<true><<<grid, 256, 0, s>>>(a);
-  else front_tiny_kernel<false><<<grid, 256, 0, s>>>(a);
+  const int slots = gate ? router_slots(gate->E_route) : 0;
+  auto go = [&](auto kern) { kern<<<grid, 256, 0, s>>>(a); };
+  switch (slots) {
+    case 0: a16 ? go(front_tiny_kernel<true, 0>) : go(front_tiny_kernel<false, 0>); break;
+    case 4: a16 ? go(front_tiny_kernel<true, 4>) : go(front_tiny_kernel<false, 4>); break;
+    case 8: a16 ? go(front_tiny_kernel<true, 8>) : go(front_tiny_kernel<false, 8>); break;
+    case 12: a16 ? go(front_tiny_kernel<true, 12>) : go(front_tiny_kernel<false, 12>); break;
+    default: a16 ? go(front_tiny_kernel<true, 16>) : go(front_tiny_kernel<false, 16>);
+  }
   return cudaGetLastError();
 }
 

@@ -243,6 +243,41 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
                                 void* out, void* ws, size_t ws_bytes, int block_m,
                                 moe_stream_t stream);
 
+/* ------------------------------------------------------- gated calls
+ * fused_moe_a8w4_gated / fused_moe_a16w4_gated: the fused calls with the
+ * gating in front (the pages time the local MoE "including gating", AITER
+ * #5609 "Add DeepSeek V4.1 Flash TP4 gfx950 MoE tuning", Performance on the
+ * measured runtime). The routing is that of moe_router_topk on
+ * router_logits (float32 [M, E_route], row stride ld >= E_route): per token
+ * the topk largest logits (ties to the lower expert), weights = softmax over
+ * the picks, and with shared_id >= 0 a last column shared_id of weight 1.0.
+ * It is written to topk_ids (int32) / topk_weights (float) [M, k'] with
+ * k' = topk + (shared_id >= 0), caller-allocated device buffers, and the
+ * layer then computes exactly what fused_moe_* computes with those ids and
+ * weights and topk = k' (ids outside [0, E) are dropped; expert-parallel
+ * shards pass the global logits). Up to 256 routes (M * k') the gating runs
+ * inside the call's first kernel, together with the sort and the gather;
+ * beyond that the gating kernel is its own launch.
+ * Workspace: fused_moe_workspace_bytes(M, H, Ip, E, k', a16).
+ * Errors: MOE_ERR_INVALID_ARG for ld < E_route, topk outside [1, E_route],
+ * shared_id >= 0 outside [E_route, 512), NULL logits / id / weight buffers
+ * with M > 0, and the errors of fused_moe_a8w4; MOE_ERR_UNSUPPORTED for
+ * E_route > 512 or k' > 16; MOE_ERR_ALIGNMENT for pointers not 256-byte
+ * aligned. All before any launch.
+ */
+moe_status_t fused_moe_a8w4_gated(const void* x, const float* router_logits, int ld, int E_route,
+                                  int topk, int shared_id, int M, int H, const uint8_t* w1,
+                                  const uint8_t* w1_scale, const uint8_t* w2,
+                                  const uint8_t* w2_scale, int E, int Ip, void* out,
+                                  int32_t* topk_ids, float* topk_weights, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream);
+moe_status_t fused_moe_a16w4_gated(const void* x, const float* router_logits, int ld,
+                                   int E_route, int topk, int shared_id, int M, int H,
+                                   const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
+                                   const uint8_t* w2_scale, int E, int Ip, void* out,
+                                   int32_t* topk_ids, float* topk_weights, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------ no-allocation variant
  * fused_moe_a8w4_noalloc: fused_moe_a8w4 without a caller workspace. The
  * pages have no counterpart of this entry point; it exists for callers that

@@ -134,6 +134,25 @@ def test_explicit_block_m_validation(L):
     assert L.fused_moe_a16w4_bm(*args, 512, None) == 2
 
 
+@pytest.mark.parametrize("fn", ["fused_moe_a8w4_gated", "fused_moe_a16w4_gated"])
+def test_gated_rejects_bad_arguments_on_host(L, fn):
+    def call(M=4, ld=384, E_route=384, topk=6, shared=-1, lg=FAKE, ids=FAKE, w=FAKE, E=384,
+             H=256, Ip=128, ws=FAKE, ws_bytes=1 << 40):
+        return getattr(L, fn)(FAKE, lg, ld, E_route, topk, shared, M, H, FAKE, FAKE, FAKE, FAKE,
+                              E, Ip, FAKE, ids, w, ws, ws_bytes, None)
+    assert call(ld=100) == 1                   # ld < E_route
+    assert call(topk=0) == 1 and call(topk=385) == 1
+    assert call(shared=10) == 1                # a routed expert as the shared one
+    assert call(shared=512) == 1
+    assert call(lg=None) == 1 and call(ids=None) == 1 and call(w=None) == 1
+    assert call(E_route=600, ld=600) == 2      # > 512 routed experts
+    assert call(topk=16, shared=384) == 2      # 17 columns
+    assert call(ids=FAKE + 8) == 4             # misaligned
+    assert call(ws_bytes=16) == 3              # workspace too small
+    assert call(H=200) == 2                    # the fused call's own checks
+    assert call(M=0, lg=None, ids=None, w=None) == 0   # empty call, no launch
+
+
 def test_noalloc_status_rejects_bad_arguments_on_host(L):
     assert L.moe_noalloc_status(None, None) == 1
     assert L.moe_noalloc_status(FAKE + 4, None) == 4

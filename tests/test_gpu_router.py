@@ -12,7 +12,7 @@ import torch
 
 import block_scaled_moe_sort_gb300 as m
 import moe_inputs as mi
-from moe_check import compare
+from moe_check import check_outputs, compare, sample_tokens, weights_for, layer_for
 from oracle import router as orr
 
 pytestmark = pytest.mark.gpu
@@ -89,3 +89,99 @@ def test_separate_shared_expert(cuda_lib, a16):
     case.topk_ids = ids_c
     case.topk_weights = wt_c
     print(compare(case, layer, a16))
+
+
+# ------------------------------------------------------------ gated calls
+# fused_moe_*_gated: the gating (the same selection and softmax as
+# moe_router_topk) in front of the fused call; up to 256 routes it runs
+# inside the decode front kernel, beyond that as its own launch.
+
+def _gated_check(layer, case, logits, topk, a16, shared=None, tokens=None):
+    M = case.M
+    x = case.x.cuda()
+    lg = logits.cuda()
+    kout = topk + (1 if shared is not None else 0)
+    ws = torch.empty(layer.workspace_bytes(M, kout), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)
+    out = torch.empty(M, layer.H, dtype=torch.bfloat16, device="cuda")
+    out.view(torch.int16).fill_(-1)
+    out, ids, w = m.fused_moe_gated(x, lg, topk, layer.w1, layer.w1_scale, layer.w2,
+                                    layer.w2_scale, layer.E, layer.Ip, a16=a16, shared_id=shared,
+                                    out=out, ws=ws)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = orr.router_topk(logits.numpy(), topk, shared_id=shared)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.cpu().numpy().astype(np.float64), ref_w, rtol=RTOL, atol=0)
+    # the layer's result on the routing it produced, against the oracle
+    case.topk_ids = ids.cpu()
+    case.topk_weights = w.cpu()
+    return check_outputs(case, layer, a16, out, ws, tokens=tokens)
+
+
+@pytest.mark.parametrize("name,M", [("backbone", 6), ("backbone", 24), ("draft", 5),
+                                    ("ep", 16), ("a16w4_384", 12)])
+def test_gated_call_decode(cuda_lib, name, M):
+    # at most 256 routes: gating, sort and gather in the call's first kernel
+    shp = mi.SHAPES[name]
+    layer = layer_for(name)
+    case = mi.make_case(name, M, weights=weights_for(name))
+    logits = _logits(M, shp.E_route, 4000 + M)
+    print(_gated_check(layer, case, logits, shp.topk, shp.a16))
+
+
+def test_gated_call_shared_expert_decode(cuda_lib):
+    # 384 routed experts top-6 plus the shared expert 384 (7 columns)
+    layer = layer_for("a16w4_385")
+    case = mi.make_case("a16w4_385", 12, weights=weights_for("a16w4_385"))
+    logits = _logits(12, 384, 4100)
+    print(_gated_check(layer, case, logits, 6, True, shared=384))
+
+
+@pytest.mark.parametrize("a16", [False, True])
+def test_gated_call_separate_launch(cuda_lib, a16):
+    # more than 256 routes: the gating kernel runs as its own launch
+    shp = mi.small_shape(H=512, I=192, Ip=256, E=8, topk=3, E_route=8, a16=a16)
+    w = mi.make_weights(shp, 23)
+    layer = m.MoeLayer(w["w1"], w["w1_scale"], w["w2"], w["w2_scale"], a16=a16)
+    case = mi.make_case("small", 130, shape=shp, weights=w)
+    print(_gated_check(layer, case, _logits(130, 8, 4200), 3, a16))
+
+
+def test_gated_call_prefill_sample(cuda_lib):
+    layer = layer_for("backbone")
+    case = mi.make_case("backbone", 4096, weights=weights_for("backbone"))
+    logits = _logits(4096, 384, 4300)
+    print(_gated_check(layer, case, logits, 6, False, tokens=sample_tokens(4096, 8, 5)))
+
+
+def test_gated_call_graph_replay_changed_logits(cuda_lib):
+    # one captured gated call, replayed on new logits written in place
+    layer = layer_for("backbone")
+    M = 12
+    x = mi.make_case("backbone", M, weights=weights_for("backbone")).x.cuda()
+    lg = _logits(M, 384, 4400).cuda()
+    out = torch.empty(M, layer.H, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(M, 6, dtype=torch.int32, device="cuda")
+    w = torch.empty(M, 6, dtype=torch.float32, device="cuda")
+    ws = torch.empty(layer.workspace_bytes(M, 6), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.forward_gated(x, lg, 6, out=out, ws=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        m.fused_moe_gated(x, lg, 6, layer.w1, layer.w1_scale, layer.w2, layer.w2_scale, layer.E,
+                          layer.Ip, out=out, ws=ws, topk_ids=ids, topk_weights=w, stream=s)
+    for seed in (4401, 4402):
+        new = _logits(M, 384, seed)
+        lg.copy_(new)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref_ids, _ = orr.router_topk(new.numpy(), 6)
+        assert np.array_equal(ids.cpu().numpy(), ref_ids)
+        case = mi.make_case("backbone", M, weights=weights_for("backbone"))
+        case.topk_ids = ids.cpu()
+        case.topk_weights = w.cpu()
+        print(check_outputs(case, layer, False, out, ws))
+    del g
