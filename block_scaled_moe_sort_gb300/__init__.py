@@ -22,7 +22,7 @@ __all__ = [
     "moe_prepack_scales_mx", "moe_prepack_weights_mx", "fused_moe_workspace_bytes", "fused_moe_workspace_layout",
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
     "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS", "fused_moe_a8w4_noalloc",
-    "moe_noalloc_status", "fused_moe_gated",
+    "moe_noalloc_status", "fused_moe_gated", "shared_expert_pieces", "with_shared_expert",
 ]
 
 HEADER = os.path.join(_build.ROOT, "include", "moe_mx.h")
@@ -53,8 +53,8 @@ _SIGS = {
                           _c_size_t, _c_void_p]),
     "moe_quant_act_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_void_p,
                                   _c_void_p]),
-    "moe_router_topk": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_void_p,
-                                 _c_void_p, _c_void_p]),
+    "moe_router_topk": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                 _c_void_p, _c_void_p, _c_void_p]),
     "moe_prepacked_scale_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
     "moe_prepacked_weight_bytes": (_c_size_t, [_c_int, _c_int, _c_int]),
     "moe_prepack_weights_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p,
@@ -82,14 +82,10 @@ _SIGS = {
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
                                         _c_int, _c_void_p, _c_void_p]),
     "moe_noalloc_status": (_c_int, [_c_void_p, _c_void_p]),
-    "fused_moe_a8w4_gated": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int,
-                                      _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int,
-                                      _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
-                                      _c_size_t, _c_void_p]),
-    "fused_moe_a16w4_gated": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int,
-                                       _c_int, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
-                                       _c_int, _c_int, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
-                                       _c_size_t, _c_void_p]),
+    "fused_moe_a8w4_gated": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 7 + [_c_void_p] * 4 +
+                               [_c_int, _c_int] + [_c_void_p] * 4 + [_c_size_t, _c_void_p]),
+    "fused_moe_a16w4_gated": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 7 + [_c_void_p] * 4 +
+                               [_c_int, _c_int] + [_c_void_p] * 4 + [_c_size_t, _c_void_p]),
     "moe_profile_enable": (_c_int, [_c_int]),
     "moe_profile_collect": (_c_int, [ctypes.POINTER(ctypes.c_double),
                                      ctypes.POINTER(ctypes.c_int32)]),
@@ -205,17 +201,18 @@ def moe_debug_wait_selftest(timeout_us: int = 1000, device="cuda", stream=None):
 # ---------------------------------------------------------------- gating
 
 def moe_router_topk(logits: torch.Tensor, topk: int, shared_id: Optional[int] = None,
-                    stream=None):
+                    stream=None, n_shared: int = 1):
     """Router logits float32 [M, E] -> (topk_ids int32 [M, k'], topk_weights
-    float32 [M, k']), k' = topk (+1 with a shared expert of weight 1)."""
+    float32 [M, k']), k' = topk (+ n_shared shared-expert columns of weight 1,
+    ids shared_id, shared_id + 1, ...)."""
     assert logits.dtype == torch.float32 and logits.dim() == 2 and logits.stride(1) == 1
     M, E = logits.shape
-    kout = topk + (1 if shared_id is not None else 0)
+    kout = topk + (n_shared if shared_id is not None else 0)
     ids = torch.empty(M, kout, dtype=torch.int32, device=logits.device)
     w = torch.empty(M, kout, dtype=torch.float32, device=logits.device)
     _check("moe_router_topk", lib().moe_router_topk(
         _ptr(logits), M, E, logits.stride(0), topk, -1 if shared_id is None else shared_id,
-        _ptr(ids), _ptr(w), _stream(stream)))
+        n_shared, _ptr(ids), _ptr(w), _stream(stream)))
     return ids, w
 
 
@@ -328,14 +325,14 @@ def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_pa
 
 def fused_moe_gated(x, router_logits, topk, w1_packed, w1_scale_packed, w2_packed,
                     w2_scale_packed, E, Ip, a16=False, shared_id=None, out=None, ws=None,
-                    topk_ids=None, topk_weights=None, stream=None):
+                    topk_ids=None, topk_weights=None, stream=None, n_shared: int = 1):
     """The fused call with the gating in front: router logits float32
     [M, E_route] -> (out BF16 [M, H], topk_ids int32 [M, k'], topk_weights
-    float32 [M, k']), k' = topk (+1 with a shared expert)."""
+    float32 [M, k']), k' = topk (+ n_shared shared-expert columns)."""
     M, H = x.shape
     assert router_logits.dtype == torch.float32 and router_logits.stride(1) == 1
     E_route = router_logits.shape[1]
-    kout = topk + (1 if shared_id is not None else 0)
+    kout = topk + (n_shared if shared_id is not None else 0)
     dev = x.device
     if out is None:
         out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
@@ -349,7 +346,8 @@ def fused_moe_gated(x, router_logits, topk, w1_packed, w1_scale_packed, w2_packe
     fn = "fused_moe_a16w4_gated" if a16 else "fused_moe_a8w4_gated"
     code = getattr(lib(), fn)(
         _ptr(x), _ptr(router_logits), router_logits.stride(0), E_route, topk,
-        -1 if shared_id is None else shared_id, M, H, _ptr(w1_packed), _ptr(w1_scale_packed),
+        -1 if shared_id is None else shared_id, n_shared, M, H, _ptr(w1_packed),
+        _ptr(w1_scale_packed),
         _ptr(w2_packed), _ptr(w2_scale_packed), E, Ip, _ptr(out), _ptr(topk_ids),
         _ptr(topk_weights), _ptr(ws), ws.numel(), _stream(stream))
     _check(fn, code)
@@ -401,19 +399,48 @@ def moe_profile_collect() -> tuple:
     return dict(zip(PROFILE_SLOTS, list(ms))), int(n.value)
 
 
+def shared_expert_pieces(shared, Ip: int):
+    """One shared expert (w1 [2*Is, H/2], w1_scale [2*Is, H/32], w2 [H, Is/2],
+    w2_scale [H, Is/32], or the same with a leading dimension of 1) as
+    ceil(Is / Ip) experts of the routed intermediate size Ip: piece j holds
+    intermediate indices [j*Ip, (j+1)*Ip) - gate/up rows of w1 and columns of
+    w2 - zero-padded at the end. SiLU(gate)*up acts on each intermediate index
+    alone and the down projection sums over them, so running the pieces as
+    experts of weight 1 and adding them gives the shared MLP (Ip is a multiple
+    of 32: no 1x32 block of the intermediate straddles two pieces).
+    Load-time data preparation; returns [n, ...] tensors."""
+    w1, s1, w2, s2 = (t[0] if t.dim() == 3 else t for t in shared)
+    Is = w2.shape[1] * 2
+    if Is % 32 or w1.shape[0] != 2 * Is or s1.shape[0] != 2 * Is or s2.shape[1] * 32 != Is:
+        raise ValueError(f"inconsistent shared expert shapes for intermediate size {Is}")
+    n = -(-Is // Ip)
+    p1 = torch.zeros(n, 2 * Ip, w1.shape[1], dtype=torch.uint8)
+    q1 = torch.zeros(n, 2 * Ip, s1.shape[1], dtype=torch.uint8)
+    p2 = torch.zeros(n, w2.shape[0], Ip // 2, dtype=torch.uint8)
+    q2 = torch.zeros(n, w2.shape[0], Ip // 32, dtype=torch.uint8)
+    for j in range(n):
+        lo, hi = j * Ip, min((j + 1) * Ip, Is)
+        p1[j, :2 * (hi - lo)] = w1[2 * lo:2 * hi].cpu()
+        q1[j, :2 * (hi - lo)] = s1[2 * lo:2 * hi].cpu()
+        p2[j, :, :(hi - lo) // 2] = w2[:, lo // 2:hi // 2].cpu()
+        q2[j, :, :(hi - lo) // 32] = s2[:, lo // 32:hi // 32].cpu()
+    return p1, q1, p2, q2
+
+
 def with_shared_expert(w1, w1_scale, w2, w2_scale, shared):
-    """Routed expert tensors [E, ...] plus one separate shared expert's
-    (w1 [2*Ip, H/2] or [1, 2*Ip, H/2], its scales, w2, its scales) -> the
-    same tensors with the shared expert appended as expert E (load-time data
-    preparation before the one-time prepack)."""
+    """Routed expert tensors [E, ...] plus one separate shared expert of any
+    intermediate size -> the same tensors with the shared expert's pieces
+    (shared_expert_pieces) appended as experts E, E+1, ..., and the number of
+    pieces (load-time data preparation before the one-time prepack)."""
+    Ip = w2.shape[2] * 2
+    pieces = shared_expert_pieces(shared, Ip)
     out = []
-    for routed, sh in zip((w1, w1_scale, w2, w2_scale), shared):
-        sh = sh if sh.dim() == routed.dim() else sh.unsqueeze(0)
-        if sh.shape[0] != 1 or sh.shape[1:] != routed.shape[1:]:
-            raise ValueError(f"shared expert tensor of shape {tuple(sh.shape)} does not match "
+    for routed, sh in zip((w1, w1_scale, w2, w2_scale), pieces):
+        if sh.shape[1:] != routed.shape[1:]:
+            raise ValueError(f"shared expert piece of shape {tuple(sh.shape)} does not match "
                              f"routed experts {tuple(routed.shape)}")
         out.append(torch.cat([routed, sh.to(routed.device, routed.dtype)], dim=0))
-    return tuple(out)
+    return (*out, pieces[0].shape[0])
 
 
 def shipped_block_m_rows(H: int, Ip: int, E: int, a16: bool) -> dict:
@@ -440,19 +467,23 @@ class MoeLayer:
 
     shared_expert: (w1, w1_scale, w2, w2_scale) of one separate shared
     expert that every token uses with weight 1 (the shared-first layouts of
-    the pages: the 385-expert top-7 case). It is appended as expert E and
-    runs inside the same grouped GEMMs as the routed experts; ``route``
-    produces ids and weights with its column, which the call takes as they
-    are."""
+    the pages: the 385-expert top-7 case), MXFP4 like the routed experts,
+    of any intermediate size Is (a multiple of 32). It is appended as
+    ceil(Is / Ip) experts E, E+1, ... (its pieces, shared_expert_pieces) and
+    runs inside the same grouped GEMMs as the routed experts; the tile walk
+    schedules the last experts' route blocks first, so the shared expert's
+    tiles lead both stages. ``route`` and ``forward_gated`` produce ids and
+    weights with its columns, which the call takes as they are."""
 
     def __init__(self, w1, w1_scale, w2, w2_scale, a16: bool = False, device="cuda",
                  block_m_table=None, shared_expert=None):
         self.a16 = a16
         self.E_routed = w1.shape[0]
         self.shared_id = None
+        self.n_shared = 0
         if shared_expert is not None:
-            w1, w1_scale, w2, w2_scale = with_shared_expert(w1, w1_scale, w2, w2_scale,
-                                                            shared_expert)
+            w1, w1_scale, w2, w2_scale, self.n_shared = with_shared_expert(
+                w1, w1_scale, w2, w2_scale, shared_expert)
             self.shared_id = self.E_routed
         self.E = w1.shape[0]
         self.H = w2.shape[1]
@@ -473,7 +504,8 @@ class MoeLayer:
         """Router logits float32 [M, E_routed] -> (topk_ids, topk_weights) for
         this layer, with the shared expert's column when it has one."""
         assert logits.shape[1] == self.E_routed
-        return moe_router_topk(logits, topk, shared_id=self.shared_id, stream=stream)
+        return moe_router_topk(logits, topk, shared_id=self.shared_id, stream=stream,
+                               n_shared=max(self.n_shared, 1))
 
     def forward_gated(self, x, router_logits, topk: int, out=None, ws=None, stream=None):
         """Gating + fused call in one (fused_moe_*_gated): router logits
@@ -483,7 +515,8 @@ class MoeLayer:
         dropped)."""
         return fused_moe_gated(x, router_logits, topk, self.w1, self.w1_scale, self.w2,
                                self.w2_scale, self.E, self.Ip, a16=self.a16,
-                               shared_id=self.shared_id, out=out, ws=ws, stream=stream)
+                               shared_id=self.shared_id, out=out, ws=ws, stream=stream,
+                               n_shared=max(self.n_shared, 1))
 
     def block_m_for(self, M: int, topk: Optional[int] = None) -> int:
         """Route block for an M-token call (0 = the library's rule)."""

@@ -71,6 +71,7 @@ struct Bf16Args {
   int n_group_log2;            // stage 2: log2 of the feature tiles per walk group
   int local;                   // derive the route layout from topk_ids (decode sizes)
   const int32_t* topk_ids;
+  LocalGate gate;        // gated calls: the routing input is the router logits
   const int32_t* sorted_route;
   const float* sorted_w;
   const int32_t* block_expert;
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   if (a.local) {
     // the epilogue's transpose buffer is free until the first tile's epilogue
     const int nb = local_block_layout(a.topk_ids, a.M * a.topk, a.E, BN,
-                                      reinterpret_cast<int*>(epi), s_blk_expert);
+                                      reinterpret_cast<int*>(epi), s_blk_expert, a.gate, a.M);
     if (threadIdx.x == 0) s_nblk = nb;
   }
   tc_fence_before();
@@ -723,9 +724,11 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.n_tiles = a.N / kTileN;
   a.num_blocks = static_cast<int>(g.p_max / g.bm);
   a.n_group_log2 = stage == 1 ? 0 : stage2_n_group_log2(g.M, g.p_max * g.Ip * 2, a.n_tiles);
-  a.local = g.topk_ids && static_cast<int64_t>(g.M) * g.topk <= kLocalMaxRoutes &&
+  a.local = (g.topk_ids || g.gate.logits) &&
+            static_cast<int64_t>(g.M) * g.topk <= kLocalMaxRoutes &&
             a.num_blocks <= kLocalMaxBlocks ? 1 : 0;
   a.topk_ids = g.topk_ids;
+  a.gate = g.gate;
   a.sorted_route = g.sorted_route; a.sorted_w = g.sorted_w; a.block_expert = g.block_expert;
   a.num_padded = g.num_padded;
   a.sfa = stage == 1 ? g.w1s : g.w2s;

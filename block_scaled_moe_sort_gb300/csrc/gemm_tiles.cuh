@@ -7,6 +7,8 @@
 #pragma once
 #include <cstdint>
 #include "common.cuh"
+#include "moe_internal.h"
+#include "router_warp.cuh"
 #include "sm100_ptx.cuh"
 
 namespace moe {
@@ -41,13 +43,39 @@ __device__ __forceinline__ int expert_checked(const Args& a, int e) {
 constexpr int kLocalMaxRoutes = 160;
 constexpr int kLocalMaxBlocks = 1024;   // R / 16 + E <= 288 + 512 at the route limit
 
+// Gated calls (gate.logits set): the routing comes from the router logits,
+// the call's input, through the per-token selection the gating kernels use.
 // All threads of the CTA; cnt: E + 1 ints of scratch shared memory (free
-// before the dependency wait); blk_expert: kLocalMaxBlocks entries. Returns
-// the number of route blocks. Contains __syncthreads.
+// before the dependency wait), followed by room for R ids when gating;
+// blk_expert: kLocalMaxBlocks entries. Returns the number of route blocks.
+// Contains __syncthreads.
 __device__ __forceinline__ int local_block_layout(const int32_t* ids, int R, int E, int bn,
-                                                  int* cnt, uint16_t* blk_expert) {
+                                                  int* cnt, uint16_t* blk_expert,
+                                                  const LocalGate& gate, int M) {
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
   for (int e = tid; e <= E; e += nt) cnt[e] = 0;
+  if (gate.logits) {
+    // one warp per token selects its experts; the ids go to shared memory
+    int* sid = cnt + E + 1;
+    const int k = R / M;
+    for (int t = tid >> 5; t < M; t += nt >> 5) {
+      uint32_t v[16];
+      router_load<16>(gate.logits + static_cast<int64_t>(t) * gate.ld, gate.E_route, lane, v);
+      int e;
+      float w;
+      router_select<16>(v, gate.topk_sel, lane, &e, &w);
+      if (lane >= gate.topk_sel && lane < gate.topk_sel + gate.n_shared)
+        e = gate.shared_id + lane - gate.topk_sel;
+      if (lane < k) sid[t * k + lane] = e;
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += nt) {
+      const int v = sid[r];
+      if (v >= 0 && v < E) atomicAdd(&cnt[v], 1);
+    }
+    ids = nullptr;
+    R = 0;   // counted
+  }
   __syncthreads();
   // 16-byte loads, four in flight per thread before any count is added
   // (topk_ids is 256-byte aligned: the library checks every pointer)
@@ -114,9 +142,13 @@ __device__ __forceinline__ void tile_coords(int t, const Args& a, int& m_blk, in
 
 // This CTA's tiles t = blockIdx.x + i * gridDim.x that hold routes, in order.
 // A tile holds routes iff its route block starts below the padded route count,
-// so the walk needs no memory access. With kExpert (the producer, the only
-// role that addresses weights) the expert id of the next tile is loaded one
-// tile ahead, off its critical path; the other roles never load it (e = 0).
+// so the walk needs no memory access. Route blocks are walked from the last
+// one down: shared experts are appended after the routed ones, so their
+// blocks (every token's route, the largest segments) are scheduled first,
+// and the longest work starts in the first wave. With kExpert (the
+// producer, the only role that addresses weights) the expert id of the next
+// tile is loaded one tile ahead, off its critical path; the other roles
+// never load it (e = 0).
 template <class Args, bool kExpert = true>
 struct TileSeq {
   int t, m_blk, n_tile, e;
@@ -128,7 +160,10 @@ struct TileSeq {
                                               int P, int bn) {
     for (; t < total; t += gridDim.x) {
       tile_coords(t, a, m, n);
-      if (m * bn < P) return true;
+      if (m * bn < P) {
+        m = P / bn - 1 - m;   // last route block first
+        return true;
+      }
     }
     return false;
   }
@@ -169,7 +204,7 @@ struct SplitSeq {
   bool valid;
   int nt, nm, nn, ne, nkb0, nkb1, nslot;
   bool nvalid;
-  int wg, S, U, kblocks;
+  int wg, S, U, kblocks, pblk;
 
   __device__ __forceinline__ bool locate(int u, int& m, int& n, int& k0, int& k1, int& sl,
                                          const Args& a) const {
@@ -184,13 +219,14 @@ struct SplitSeq {
       k1 = (part + 1) * kblocks / S;
       sl = v / S;
     }
-    m = tt / a.n_tiles;
+    m = pblk - 1 - tt / a.n_tiles;   // last route block first
     n = tt % a.n_tiles;
     return true;
   }
   __device__ __forceinline__ void init(const Args& a, int P, int bn, int kb) {
     kblocks = kb;
-    const int T = (P / bn) * a.n_tiles;
+    pblk = P / bn;
+    const int T = pblk * a.n_tiles;
     const int G = gridDim.x;
     const int W = T / G, r = T - W * G;
     int parts = 1;

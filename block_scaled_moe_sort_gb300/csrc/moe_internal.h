@@ -7,6 +7,13 @@
 
 namespace moe {
 
+// Gating input of a GEMM's local route layout (gated calls): router logits
+// [M, ld] of E_route experts, topk_sel picks plus n_shared shared columns.
+struct LocalGate {
+  const float* logits;
+  int ld, E_route, topk_sel, shared_id, n_shared;
+};
+
 // Sets the dynamic shared-memory limit of `func` once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes);
 
@@ -23,7 +30,8 @@ cudaError_t launch_quant_act(const void* x, int M, int K, int ldx, uint8_t* q, u
 cudaError_t launch_wait_selftest(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 cudaError_t launch_router_topk(const float* logits, int M, int E, int ld, int topk,
-                               int shared_id, int32_t* ids, float* weights, cudaStream_t s);
+                               int shared_id, int n_shared, int32_t* ids, float* weights,
+                               cudaStream_t s);
 
 cudaError_t launch_prepack_weights(const uint8_t* w, int E, int N, int K, uint8_t* out,
                                    cudaStream_t s);
@@ -32,11 +40,12 @@ cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uin
 
 // Gating inside the decode front kernel (the gated calls): router logits
 // [M, ld] of E_route experts; topk_sel picks per token plus, with
-// shared_id >= 0, the shared expert column; the ids and weights are written
-// to ids_out / w_out [M, topk] as well.
+// shared_id >= 0, n_shared shared-expert columns (ids shared_id,
+// shared_id + 1, ..., weight 1); the ids and weights are written to
+// ids_out / w_out [M, topk] as well.
 struct FrontGating {
   const float* logits;
-  int ld, E_route, topk_sel, shared_id;
+  int ld, E_route, topk_sel, shared_id, n_shared;
   int32_t* ids_out;
   float* w_out;
 };
@@ -66,6 +75,7 @@ struct GemmArgs {
   int M, H, Ip, E, topk, bm;
   int64_t p_max;
   const int32_t* topk_ids;   // the call's routing input (local layout at decode sizes)
+  LocalGate gate;            // gated calls: router logits instead (topk_ids is then null)
   const int32_t* sorted_route;
   const float* sorted_w;
   const int32_t* block_expert;

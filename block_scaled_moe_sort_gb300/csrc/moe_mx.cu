@@ -186,7 +186,7 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
     prof_mark(0, true, s);
     if (gate) {
       e = launch_router_topk(gate->logits, M, gate->E_route, gate->ld, gate->topk_sel,
-                             gate->shared_id, gate->ids_out, gate->w_out, s);
+                             gate->shared_id, gate->n_shared, gate->ids_out, gate->w_out, s);
       if (e != cudaSuccess) return from_cuda(e);
     }
     int32_t* sort_scratch = reinterpret_cast<int32_t*>(base + L.sort_scratch_off);
@@ -207,6 +207,9 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   // the GEMMs may read topk_ids before their dependency wait only when it is
   // an input of the call (not when the gating kernel writes it)
   g.topk_ids = gate ? nullptr : ids;
+  g.gate = gate ? LocalGate{gate->logits, gate->ld, gate->E_route, gate->topk_sel,
+                            gate->shared_id, gate->n_shared}
+                : LocalGate{nullptr, 0, 0, 0, -1, 0};
   g.sorted_route = sorted_route; g.sorted_w = sorted_w; g.block_expert = block_expert;
   g.num_padded = num_padded;
   g.w1 = w1; g.w1s = w1s; g.w2 = w2; g.w2s = w2s;
@@ -296,17 +299,21 @@ moe_status_t moe_quant_act_mx(const void* x_bf16, int M, int K, int ldx, uint8_t
 }
 
 moe_status_t moe_router_topk(const float* logits, int M, int E, int ld, int topk, int shared_id,
-                             int32_t* topk_ids, float* topk_weights, moe_stream_t stream) {
+                             int n_shared, int32_t* topk_ids, float* topk_weights,
+                             moe_stream_t stream) {
   if (M < 0 || E <= 0 || ld < E || topk < 1 || topk > E) return MOE_ERR_INVALID_ARG;
   // a shared expert is an extra expert after the routed ones: an id among
   // them would double-count a pick, one beyond the sort's range would be
   // dropped silently
-  if (shared_id >= 0 && (shared_id < E || shared_id >= kMaxExperts)) return MOE_ERR_INVALID_ARG;
-  if (E > kMaxExperts || topk + (shared_id >= 0 ? 1 : 0) > kMaxTopk) return MOE_ERR_UNSUPPORTED;
+  if (shared_id >= 0 && (shared_id < E || n_shared < 1 || shared_id + n_shared > kMaxExperts))
+    return MOE_ERR_INVALID_ARG;
+  if (shared_id < 0) n_shared = 0;
+  if (E > kMaxExperts || topk + n_shared > kMaxTopk) return MOE_ERR_UNSUPPORTED;
   if (M > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
   if (M > 0 && (!aligned(logits) || !aligned(topk_ids) || !aligned(topk_weights)))
     return MOE_ERR_ALIGNMENT;
-  return from_cuda(launch_router_topk(logits, M, E, ld, topk, shared_id, topk_ids, topk_weights,
+  return from_cuda(launch_router_topk(logits, M, E, ld, topk, shared_id, n_shared, topk_ids,
+                                      topk_weights,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -401,21 +408,22 @@ moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids, const float
 
 namespace {
 moe_status_t gated_call(bool a16, const void* x, const float* logits, int ld, int E_route,
-                        int topk, int shared_id, int M, int H, const uint8_t* w1,
+                        int topk, int shared_id, int n_shared, int M, int H, const uint8_t* w1,
                         const uint8_t* w1_scale, const uint8_t* w2, const uint8_t* w2_scale,
                         int E, int Ip, void* out, int32_t* topk_ids, float* topk_weights,
                         void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (M < 0 || E_route <= 0 || ld < E_route || topk < 1 || topk > E_route)
     return MOE_ERR_INVALID_ARG;
-  if (shared_id >= 0 && (shared_id < E_route || shared_id >= kMaxExperts))
+  if (shared_id >= 0 && (shared_id < E_route || n_shared < 1 || shared_id + n_shared > kMaxExperts))
     return MOE_ERR_INVALID_ARG;
+  if (shared_id < 0) n_shared = 0;
   if (E_route > kMaxExperts) return MOE_ERR_UNSUPPORTED;
-  const int kout = topk + (shared_id >= 0 ? 1 : 0);
+  const int kout = topk + n_shared;
   if (kout > kMaxTopk) return MOE_ERR_UNSUPPORTED;
   if (M > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
   if (M > 0 && (!aligned(logits) || !aligned(topk_ids) || !aligned(topk_weights)))
     return MOE_ERR_ALIGNMENT;
-  FrontGating gate{logits, ld, E_route, topk, shared_id, topk_ids, topk_weights};
+  FrontGating gate{logits, ld, E_route, topk, shared_id, n_shared, topk_ids, topk_weights};
   return fused_moe_impl(a16, x, topk_ids, topk_weights, M, H, kout, w1, w1_scale, w2, w2_scale,
                         E, Ip, out, ws, ws_bytes, 0, reinterpret_cast<cudaStream_t>(stream),
                         &gate);
@@ -423,23 +431,26 @@ moe_status_t gated_call(bool a16, const void* x, const float* logits, int ld, in
 }  // namespace
 
 moe_status_t fused_moe_a8w4_gated(const void* x, const float* router_logits, int ld, int E_route,
-                                  int topk, int shared_id, int M, int H, const uint8_t* w1,
-                                  const uint8_t* w1_scale, const uint8_t* w2,
+                                  int topk, int shared_id, int n_shared, int M, int H,
+                                  const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
                                   const uint8_t* w2_scale, int E, int Ip, void* out,
                                   int32_t* topk_ids, float* topk_weights, void* ws,
                                   size_t ws_bytes, moe_stream_t stream) {
-  return gated_call(false, x, router_logits, ld, E_route, topk, shared_id, M, H, w1, w1_scale, w2,
-                    w2_scale, E, Ip, out, topk_ids, topk_weights, ws, ws_bytes, stream);
+  return gated_call(false, x, router_logits, ld, E_route, topk, shared_id, n_shared, M, H, w1,
+                    w1_scale, w2, w2_scale, E, Ip, out, topk_ids, topk_weights, ws, ws_bytes,
+                    stream);
 }
 
 moe_status_t fused_moe_a16w4_gated(const void* x, const float* router_logits, int ld,
-                                   int E_route, int topk, int shared_id, int M, int H,
-                                   const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
+                                   int E_route, int topk, int shared_id, int n_shared, int M,
+                                   int H, const uint8_t* w1, const uint8_t* w1_scale,
+                                   const uint8_t* w2,
                                    const uint8_t* w2_scale, int E, int Ip, void* out,
                                    int32_t* topk_ids, float* topk_weights, void* ws,
                                    size_t ws_bytes, moe_stream_t stream) {
-  return gated_call(true, x, router_logits, ld, E_route, topk, shared_id, M, H, w1, w1_scale, w2,
-                    w2_scale, E, Ip, out, topk_ids, topk_weights, ws, ws_bytes, stream);
+  return gated_call(true, x, router_logits, ld, E_route, topk, shared_id, n_shared, M, H, w1,
+                    w1_scale, w2, w2_scale, E, Ip, out, topk_ids, topk_weights, ws, ws_bytes,
+                    stream);
 }
 
 moe_status_t moe_profile_enable(int enable) {

@@ -181,7 +181,7 @@ struct FrontArgs {
   // gated call: routing from router logits [M, ld] of E_route experts
   // (topk picks plus an optional shared expert column, a.topk columns in all)
   const float* logits;
-  int ld, E_route, topk_sel, shared_id;
+  int ld, E_route, topk_sel, shared_id, n_shared;
   int32_t* ids_out;     // [M, topk] written by CTA 0
   float* w_out;
 };
@@ -221,7 +221,10 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
       int e;
       float w;
       router_select<SLOTS>(v, a.topk_sel, lane, &e, &w);
-      if (lane == a.topk_sel && a.shared_id >= 0) { e = a.shared_id; w = 1.f; }
+      if (lane >= a.topk_sel && lane < a.topk_sel + a.n_shared) {   // shared columns
+        e = a.shared_id + lane - a.topk_sel;
+        w = 1.f;
+      }
       if (lane < a.topk) {
         const int r = tt * a.topk + lane;
         e_s[r] = e;
@@ -471,13 +474,14 @@ cudaError_t launch_front_tiny(bool a16, const void* x, const int32_t* ids, const
   FrontArgs a{ids, wts, static_cast<const __nv_bfloat16*>(x), M, H, topk, E, bm, p_max,
               sorted_route, sorted_w, block_expert, expert_off, num_padded, route_pos, status,
               act, act_sf, acc, static_cast<float4*>(zero2), zero2 ? zero2_bytes / 16 : 0,
-              nullptr, 0, 0, 0, -1, nullptr, nullptr};
+              nullptr, 0, 0, 0, -1, 0, nullptr, nullptr};
   if (gate) {
     a.logits = gate->logits;
     a.ld = gate->ld;
     a.E_route = gate->E_route;
     a.topk_sel = gate->topk_sel;
     a.shared_id = gate->shared_id;
+    a.n_shared = gate->shared_id >= 0 ? gate->n_shared : 0;
     a.ids_out = gate->ids_out;
     a.w_out = gate->w_out;
   }

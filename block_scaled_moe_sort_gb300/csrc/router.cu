@@ -31,7 +31,7 @@ constexpr int kRouterWarps = 8;                    // tokens per CTA
 template <int SLOTS>
 __global__ void __launch_bounds__(kRouterWarps * 32)
     router_topk_kernel(const float* __restrict__ logits, int M, int E, int ld, int topk,
-                       int shared_id, int kout, int32_t* __restrict__ ids,
+                       int shared_id, int n_shared, int kout, int32_t* __restrict__ ids,
                        float* __restrict__ weights) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
@@ -45,8 +45,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   if (lane < topk) {
     ids[base + lane] = e;
     weights[base + lane] = w;
-  } else if (lane == topk && shared_id >= 0) {
-    ids[base + lane] = shared_id;
+  } else if (lane < topk + n_shared) {   // the shared expert's columns
+    ids[base + lane] = shared_id + lane - topk;
     weights[base + lane] = 1.f;
   }
 }
@@ -54,26 +54,28 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 }  // namespace
 
 cudaError_t launch_router_topk(const float* logits, int M, int E, int ld, int topk,
-                               int shared_id, int32_t* ids, float* weights, cudaStream_t s) {
+                               int shared_id, int n_shared, int32_t* ids, float* weights,
+                               cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  const int kout = topk + (shared_id >= 0 ? 1 : 0);
+  if (shared_id < 0) n_shared = 0;
+  const int kout = topk + n_shared;
   const int grid = (M + kRouterWarps - 1) / kRouterWarps;
   const dim3 block(kRouterWarps * 32);
   switch (router_slots(E)) {
     case 4:
-      router_topk_kernel<4><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, kout, ids,
+      router_topk_kernel<4><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, n_shared, kout, ids,
                                                    weights);
       break;
     case 8:
-      router_topk_kernel<8><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, kout, ids,
+      router_topk_kernel<8><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, n_shared, kout, ids,
                                                    weights);
       break;
     case 12:
-      router_topk_kernel<12><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, kout, ids,
+      router_topk_kernel<12><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, n_shared, kout, ids,
                                                     weights);
       break;
     default:
-      router_topk_kernel<16><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, kout, ids,
+      router_topk_kernel<16><<<grid, block, 0, s>>>(logits, M, E, ld, topk, shared_id, n_shared, kout, ids,
                                                      weights);
   }
   return cudaGetLastError();

@@ -107,20 +107,23 @@ moe_status_t moe_sort(const int32_t* topk_ids, const float* topk_weights, int M,
  *     in ascending expert order; columns are in that order (descending
  *     logit, then ascending expert);
  *   - weight of a pick = softmax of the picks' logits (FP32 arithmetic);
- *   - if shared_id >= 0, one more column holds shared_id with weight 1.0
- *     (the 385-expert top-7 layout: the shared expert is id E).
+ *   - if shared_id >= 0, n_shared more columns hold shared_id, shared_id + 1,
+ *     ..., each with weight 1.0 (the 385-expert top-7 layout: one shared
+ *     expert, id E; a shared expert whose intermediate is split into
+ *     n_shared pieces of the routed experts' size takes n_shared ids).
  * logits: float32 [M, E], row stride ld >= E elements, finite values.
- * topk_ids int32 / topk_weights float32: [M, topk (+1 with a shared expert)],
+ * topk_ids int32 / topk_weights float32: [M, topk (+ n_shared)],
  *   caller-allocated device memory, fully written.
  * Errors (before any launch): MOE_ERR_INVALID_ARG for M < 0, E < 1, ld < E,
- * topk outside [1, E], a shared_id >= 0 outside [E, 512) (a shared expert
- * comes after the E routed experts) or a NULL pointer with M > 0;
- * MOE_ERR_UNSUPPORTED for
- * E > 512 or more than 16 output columns; MOE_ERR_ALIGNMENT for pointers not
- * 256-byte aligned. M == 0 launches nothing.
+ * topk outside [1, E], shared_id >= 0 with shared_id < E (a shared expert
+ * comes after the E routed experts), n_shared < 1 or shared_id + n_shared >
+ * 512, or a NULL pointer with M > 0; MOE_ERR_UNSUPPORTED for E > 512 or more
+ * than 16 output columns; MOE_ERR_ALIGNMENT for pointers not 256-byte
+ * aligned. n_shared is ignored when shared_id < 0. M == 0 launches nothing.
  */
 moe_status_t moe_router_topk(const float* logits, int M, int E, int ld, int topk, int shared_id,
-                             int32_t* topk_ids, float* topk_weights, moe_stream_t stream);
+                             int n_shared, int32_t* topk_ids, float* topk_weights,
+                             moe_stream_t stream);
 
 /* -------------------------------------------------------- activation quant
  * moe_quant_act_mx: x BF16 [M, K] (row stride ldx elements) -> q E4M3 codes
@@ -250,9 +253,10 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
  * measured runtime). The routing is that of moe_router_topk on
  * router_logits (float32 [M, E_route], row stride ld >= E_route): per token
  * the topk largest logits (ties to the lower expert), weights = softmax over
- * the picks, and with shared_id >= 0 a last column shared_id of weight 1.0.
- * It is written to topk_ids (int32) / topk_weights (float) [M, k'] with
- * k' = topk + (shared_id >= 0), caller-allocated device buffers, and the
+ * the picks, and with shared_id >= 0 n_shared last columns shared_id, ...,
+ * shared_id + n_shared - 1 of weight 1.0. It is written to topk_ids (int32)
+ * / topk_weights (float) [M, k'] with k' = topk + n_shared (0 shared columns
+ * when shared_id < 0), caller-allocated device buffers, and the
  * layer then computes exactly what fused_moe_* computes with those ids and
  * weights and topk = k' (ids outside [0, E) are dropped; expert-parallel
  * shards pass the global logits). Up to 256 routes (M * k') the gating runs
@@ -260,22 +264,23 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
  * beyond that the gating kernel is its own launch.
  * Workspace: fused_moe_workspace_bytes(M, H, Ip, E, k', a16).
  * Errors: MOE_ERR_INVALID_ARG for ld < E_route, topk outside [1, E_route],
- * shared_id >= 0 outside [E_route, 512), NULL logits / id / weight buffers
+ * shared_id >= 0 with shared_id < E_route, n_shared < 1 or shared_id +
+ * n_shared > 512, NULL logits / id / weight buffers
  * with M > 0, and the errors of fused_moe_a8w4; MOE_ERR_UNSUPPORTED for
  * E_route > 512 or k' > 16; MOE_ERR_ALIGNMENT for pointers not 256-byte
  * aligned. All before any launch.
  */
 moe_status_t fused_moe_a8w4_gated(const void* x, const float* router_logits, int ld, int E_route,
-                                  int topk, int shared_id, int M, int H, const uint8_t* w1,
-                                  const uint8_t* w1_scale, const uint8_t* w2,
+                                  int topk, int shared_id, int n_shared, int M, int H,
+                                  const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
                                   const uint8_t* w2_scale, int E, int Ip, void* out,
                                   int32_t* topk_ids, float* topk_weights, void* ws,
                                   size_t ws_bytes, moe_stream_t stream);
 moe_status_t fused_moe_a16w4_gated(const void* x, const float* router_logits, int ld,
-                                   int E_route, int topk, int shared_id, int M, int H,
-                                   const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,
-                                   const uint8_t* w2_scale, int E, int Ip, void* out,
-                                   int32_t* topk_ids, float* topk_weights, void* ws,
+                                   int E_route, int topk, int shared_id, int n_shared, int M,
+                                   int H, const uint8_t* w1, const uint8_t* w1_scale,
+                                   const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                                   void* out, int32_t* topk_ids, float* topk_weights, void* ws,
                                    size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------ no-allocation variant

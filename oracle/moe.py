@@ -217,3 +217,58 @@ def fused_moe(x, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, E: int,
         as_all = None if a16 else np.zeros((0, Ip // 32), dtype=np.uint8)
     return MoeResult(mx.bf16_round(out_sel), out_sel, srt, rows, aq_all, as_all, tok_sel)
 
+
+# ------------------------------------------------------- shared expert
+
+def shared_mlp(x, w1, w1_scale, w2, w2_scale, a16: bool = False) -> np.ndarray:
+    """The shared expert as a dense MLP over every token, FP64 output before
+    rounding [M, H]: the same steps as one expert of the layer (activation
+    quantisation, gate/up GEMM, SiLU(gate)*up, intermediate requantisation,
+    down projection) with routing weight 1. ``w1`` uint8 [2*Is, H/2],
+    ``w1_scale`` [2*Is, H/32], ``w2`` [H, Is/2], ``w2_scale`` [H, Is/32]; Is
+    may differ from the routed experts' intermediate size."""
+    xf = _np(x)
+    M = xf.shape[0]
+    ids = np.zeros((M, 1), dtype=np.int32)
+    w = np.ones((M, 1), dtype=np.float32)
+    W = [np.asarray(_np(a))[None] for a in (w1, w1_scale, w2, w2_scale)]
+    return fused_moe(x, ids, w, *W, 1, a16=a16).out_f64
+
+
+def fused_moe_with_shared(x, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, E: int,
+                          shared, a16: bool = False) -> np.ndarray:
+    """Routed experts plus a separate shared expert ``shared`` = (w1,
+    w1_scale, w2, w2_scale) of its own intermediate size, added with weight
+    1 to every token (the "shared expert" of AITER #5609 "Add DeepSeek V4.1
+    Flash TP4 gfx950 MoE tuning", Performance on the measured runtime): the
+    two FP64 sums are added and rounded to BF16 once. Returns BF16 values
+    (float64) [M, H]."""
+    routed = fused_moe(x, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, E, a16=a16)
+    return mx.bf16_round(routed.out_f64 + shared_mlp(x, *shared, a16=a16))
+
+
+def shared_expert_pieces(w1, w1_scale, w2, w2_scale, Ip: int):
+    """A shared expert of intermediate size Is as ceil(Is / Ip) experts of
+    intermediate size Ip: piece j holds intermediate indices [j*Ip, (j+1)*Ip)
+    (gate/up rows 2i, 2i+1 of w1, columns of w2), zero-padded at the end.
+    SiLU(gate)*up acts on each intermediate index alone and the down
+    projection sums over them, so the shared MLP is the sum of its pieces'
+    outputs; Ip is a multiple of 32, so no 1x32 block of the intermediate
+    straddles two pieces. Returns stacked [n, ...] arrays in the layer's
+    expert layout."""
+    W1, S1, W2, S2 = (np.asarray(_np(a)) for a in (w1, w1_scale, w2, w2_scale))
+    Is = W2.shape[1] * 2
+    n = -(-Is // Ip)
+    H2 = W1.shape[1]
+    p1 = np.zeros((n, 2 * Ip, H2), dtype=np.uint8)
+    q1 = np.zeros((n, 2 * Ip, S1.shape[1]), dtype=np.uint8)
+    p2 = np.zeros((n, W2.shape[0], Ip // 2), dtype=np.uint8)
+    q2 = np.zeros((n, W2.shape[0], Ip // 32), dtype=np.uint8)
+    for j in range(n):
+        lo, hi = j * Ip, min((j + 1) * Ip, Is)
+        p1[j, :2 * (hi - lo)] = W1[2 * lo:2 * hi]
+        q1[j, :2 * (hi - lo)] = S1[2 * lo:2 * hi]
+        p2[j, :, :(hi - lo) // 2] = W2[:, lo // 2:hi // 2]
+        q2[j, :, :(hi - lo) // 32] = S2[:, lo // 32:hi // 32]
+    return p1, q1, p2, q2
+

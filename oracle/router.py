@@ -19,7 +19,9 @@ and the one the synthetic routing of this repository already follows
    over the top k);
 3. optionally, a shared expert id is appended as a last column with weight
    1.0 (the 385-expert top-7 layout of AITER #6286 "Retune gfx942 a16w4
-   DSv4.1 tiles for Triton 3.8", where expert 384 is always selected).
+   DSv4.1 tiles for Triton 3.8", where expert 384 is always selected); a
+   shared expert stored as n pieces (see ``moe.shared_expert_pieces``)
+   takes n such columns, ids shared_id .. shared_id + n - 1.
 
 The selection compares the FP32 logits themselves (an ordering, exact in
 any precision); the softmax is evaluated in FP64.
@@ -31,9 +33,9 @@ from typing import Optional
 import numpy as np
 
 
-def router_topk(logits, topk: int, shared_id: Optional[int] = None):
+def router_topk(logits, topk: int, shared_id: Optional[int] = None, n_shared: int = 1):
     """logits float32 [M, E] -> (ids int32 [M, k'], weights float64 [M, k'])
-    with k' = topk (+ 1 with a shared expert)."""
+    with k' = topk (+ n_shared with a shared expert)."""
     L = np.asarray(logits, dtype=np.float32)
     M, E = L.shape
     if not 1 <= topk <= E:
@@ -47,7 +49,8 @@ def router_topk(logits, topk: int, shared_id: Optional[int] = None):
     w = e / e.sum(axis=1, keepdims=True)
     ids = order.astype(np.int32)
     if shared_id is not None:
-        # step 3: the always-selected shared expert
-        ids = np.concatenate([ids, np.full((M, 1), shared_id, dtype=np.int32)], axis=1)
-        w = np.concatenate([w, np.ones((M, 1), dtype=np.float64)], axis=1)
+        # step 3: the always-selected shared expert (its n_shared pieces)
+        sh = np.arange(shared_id, shared_id + n_shared, dtype=np.int32)
+        ids = np.concatenate([ids, np.broadcast_to(sh, (M, n_shared))], axis=1)
+        w = np.concatenate([w, np.ones((M, n_shared), dtype=np.float64)], axis=1)
     return ids, w

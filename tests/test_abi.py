@@ -106,8 +106,8 @@ def test_device_status_decoding(L):
 
 
 def test_router_rejects_bad_arguments_on_host(L):
-    def call(M=4, E=384, ld=384, k=6, shared=-1, lg=FAKE, ids=FAKE, w=FAKE):
-        return L.moe_router_topk(lg, M, E, ld, k, shared, ids, w, None)
+    def call(M=4, E=384, ld=384, k=6, shared=-1, lg=FAKE, ids=FAKE, w=FAKE, n_shared=1):
+        return L.moe_router_topk(lg, M, E, ld, k, shared, n_shared, ids, w, None)
     assert call(M=-1) == 1
     assert call(ld=100) == 1                   # ld < E
     assert call(k=0) == 1 and call(E=4, ld=4, k=5) == 1
@@ -117,6 +117,9 @@ def test_router_rejects_bad_arguments_on_host(L):
     assert call(shared=0) == 1                 # a routed expert as the shared one
     assert call(shared=383) == 1
     assert call(shared=512) == 1               # beyond the sort's expert range
+    assert call(shared=384, n_shared=0) == 1
+    assert call(shared=510, n_shared=3) == 1   # the last id beyond 511
+    assert call(k=6, shared=384, n_shared=11) == 2   # 17 columns
     assert call(w=FAKE + 4) == 4               # misaligned
     assert call(M=0, lg=None, ids=None, w=None) == 0   # empty call, no launch
 
@@ -137,13 +140,14 @@ def test_explicit_block_m_validation(L):
 @pytest.mark.parametrize("fn", ["fused_moe_a8w4_gated", "fused_moe_a16w4_gated"])
 def test_gated_rejects_bad_arguments_on_host(L, fn):
     def call(M=4, ld=384, E_route=384, topk=6, shared=-1, lg=FAKE, ids=FAKE, w=FAKE, E=384,
-             H=256, Ip=128, ws=FAKE, ws_bytes=1 << 40):
-        return getattr(L, fn)(FAKE, lg, ld, E_route, topk, shared, M, H, FAKE, FAKE, FAKE, FAKE,
-                              E, Ip, FAKE, ids, w, ws, ws_bytes, None)
+             H=256, Ip=128, ws=FAKE, ws_bytes=1 << 40, n_shared=1):
+        return getattr(L, fn)(FAKE, lg, ld, E_route, topk, shared, n_shared, M, H, FAKE, FAKE,
+                              FAKE, FAKE, E, Ip, FAKE, ids, w, ws, ws_bytes, None)
     assert call(ld=100) == 1                   # ld < E_route
     assert call(topk=0) == 1 and call(topk=385) == 1
     assert call(shared=10) == 1                # a routed expert as the shared one
     assert call(shared=512) == 1
+    assert call(shared=384, n_shared=0) == 1 and call(shared=500, n_shared=13) == 1
     assert call(lg=None) == 1 and call(ids=None) == 1 and call(w=None) == 1
     assert call(E_route=600, ld=600) == 2      # > 512 routed experts
     assert call(topk=16, shared=384) == 2      # 17 columns

@@ -305,3 +305,61 @@ def test_token_with_no_local_route_is_zero():
     none_local = (case.topk_ids >= 4).all(dim=1).numpy()
     assert none_local.any()
     assert (res.out_bf16[none_local] == 0).all()
+
+
+# ------------------------------------------------- separate shared expert
+
+def _shared_case(Is, seed):
+    shp = mi.small_shape(H=256, I=Is, Ip=Is, E=1, topk=1)
+    w = mi.make_weights(shp, seed)
+    return w["w1"][0], w["w1_scale"][0], w["w2"][0], w["w2_scale"][0]
+
+
+@pytest.mark.parametrize("Is,Ip", [(256, 128), (384, 128), (96, 128), (128, 128)])
+def test_shared_mlp_is_the_sum_of_its_pieces(Is, Ip):
+    # SiLU(gate)*up acts on each intermediate index alone and the down
+    # projection sums over them: the shared MLP equals the sum of its
+    # Ip-sized pieces run as experts of weight 1 (zero-padded at the end)
+    sh = _shared_case(Is, 31 + Is)
+    x = mi.make_x(11, 256, mi._gen(3))
+    full = om.shared_mlp(x, *sh)
+    pieces = om.shared_expert_pieces(*sh, Ip)
+    n = pieces[0].shape[0]
+    assert n == -(-Is // Ip)
+    ids = torch.arange(n, dtype=torch.int32).expand(11, n).contiguous()
+    res = om.fused_moe(x, ids, torch.ones(11, n), *pieces, n).out_f64
+    np.testing.assert_allclose(res, full, rtol=1e-12, atol=1e-12 * np.abs(full).max())
+
+
+def test_shared_mlp_is_a_dense_swiglu_mlp():
+    # brute force from the step list on a tiny shape: every token, weight 1
+    sh = _shared_case(64, 77)
+    x = mi.make_x(3, 256, mi._gen(5))
+    got = om.shared_mlp(x, *sh)
+    xq, xs = mx.quant_mxfp8(x.to(torch.float64).numpy())
+    xd = mx.dequant_mxfp8(xq, xs)
+    h = xd @ mx.dequant_mxfp4(sh[0].numpy(), sh[1].numpy()).T
+    a = h[:, 0::2] / (1 + np.exp(-h[:, 0::2])) * h[:, 1::2]
+    aq, as_ = mx.quant_mxfp8(a)
+    y = mx.dequant_mxfp8(aq, as_) @ mx.dequant_mxfp4(sh[2].numpy(), sh[3].numpy()).T
+    np.testing.assert_allclose(got, y, rtol=1e-12, atol=1e-12)
+
+
+def test_routed_plus_shared_matches_the_fused_shared_layout():
+    # with the routed size the separate shared expert equals the 385/top-7
+    # style layout: the shared expert appended as expert E with a weight-1
+    # column (both FP64 sums, one BF16 rounding)
+    shp = mi.small_shape(H=256, I=128, Ip=128, E=5, topk=2)
+    w = mi.make_weights(shp, 41)
+    case = mi.make_case("small", 9, shape=shp, weights=w)
+    sh = _shared_case(128, 43)
+    sep = om.fused_moe_with_shared(case.x, case.topk_ids, case.topk_weights, case.w1,
+                                   case.w1_scale, case.w2, case.w2_scale, 5, sh)
+    cat = [torch.cat([a, b[None]]) for a, b in zip((case.w1, case.w1_scale, case.w2,
+                                                    case.w2_scale), sh)]
+    ids = torch.cat([case.topk_ids, torch.full((9, 1), 5, dtype=torch.int32)], 1)
+    wts = torch.cat([case.topk_weights, torch.ones(9, 1)], 1)
+    fused = om.fused_moe(case.x, ids, wts, *cat, 6)
+    np.testing.assert_allclose(sep, fused.out_bf16, rtol=2 ** -7, atol=0)
+    assert (sep == fused.out_bf16).mean() > 0.99
+

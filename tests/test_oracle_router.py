@@ -96,3 +96,12 @@ def test_weights_are_shift_invariant():
 def test_rejects_bad_topk():
     with pytest.raises(ValueError):
         orr.router_topk(np.zeros((2, 4), np.float32), 5)
+
+
+def test_shared_expert_pieces_take_consecutive_columns():
+    L = np.random.default_rng(3).standard_normal((5, 12)).astype(np.float32)
+    ids1, w1 = orr.router_topk(L, 3, shared_id=12)
+    ids3, w3 = orr.router_topk(L, 3, shared_id=12, n_shared=3)
+    assert np.array_equal(ids3[:, :4], ids1) and np.array_equal(w3[:, :4], w1)
+    assert (ids3[:, 3:] == np.array([12, 13, 14])).all() and (w3[:, 3:] == 1.0).all()
+
