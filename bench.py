@@ -313,7 +313,8 @@ def measure_prefill(m, dev, stream, flush, hbm, bf16, backbone_layer, backbone_w
         else:
             weights = mi.make_weights(shape, mi.weight_seed(mi.CONFIG_INDEX[name]))
             layer = m.MoeLayer(weights["w1"], weights["w1_scale"], weights["w2"],
-                               weights["w2_scale"], a16=shape.a16, device=dev)
+                               weights["w2_scale"], a16=shape.a16, device=dev,
+                               block_m_table="gb300")
         case = mi.make_case(name, M, routing=routing, weights=weights)
         x, ids, w = case.x.to(dev), case.topk_ids.to(dev), case.topk_weights.to(dev)
         out = torch.empty(M, shape.H, dtype=torch.bfloat16, device=dev)
@@ -359,6 +360,7 @@ def config_dict(M, world, config: str = "backbone"):
     return {"workload": f"{desc}; M={M} tokens",
             "tokens": M, "H": shp.H, "I": shp.I, "Ip": shp.Ip, "experts": shp.E,
             "topk": shp.topk,
+            "route_block": "shipped GB300 tuning rows of the geometry, else the library rule",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": "flushed (256 MiB write) before every timed step"}
 
@@ -413,7 +415,7 @@ def main():
     shape = mi.SHAPES[geo]
     weights = mi.make_weights(shape, mi.weight_seed(mi.CONFIG_INDEX[geo]))
     layer = m.MoeLayer(weights["w1"], weights["w1_scale"], weights["w2"], weights["w2_scale"],
-                       a16=shape.a16, device=dev)
+                       a16=shape.a16, device=dev, block_m_table="gb300")
     case = mi.make_case(geo, args.M, routing=routing, weights=weights)
     x, ids, w = case.x.to(dev), case.topk_ids.to(dev), case.topk_weights.to(dev)
     M, k = args.M, shape.topk

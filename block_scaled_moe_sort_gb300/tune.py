@@ -34,9 +34,12 @@ from typing import Iterable, List, Optional, Sequence
 
 import os
 
-# The table measured on the GB300s for the pages' two tuned
-# geometries (backbone 384 experts top-6, draft 128 experts top-3; H=5120,
-# Ip=640; real decode rows measured per bucket as the pages do).
+# The table measured on GB300 for the pages' geometries: the two tuned
+# decode geometries (backbone 384 experts top-6, draft 128 experts top-3;
+# H=5120, Ip=640; real decode rows per bucket as the pages measure them),
+# the expert-parallel shard (96 of 384 experts, Ip=2304, routing over all
+# 384) and a16w4 (384 top-6; 385 top-7 with the shared expert as expert
+# 384; Ip=768), decode to prefill buckets.
 PACKAGED_TABLE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "block_m_gb300.csv")
 
 MIN_GAIN = 0.01
@@ -112,14 +115,24 @@ def random_layer(H: int, Ip: int, E: int, a16: bool, seed: int = 0, device: str 
     return MoeLayer(w1, w1s, w2, w2s, a16=a16, device=device)
 
 
-def random_inputs(M: int, H: int, E: int, topk: int, seed: int = 0, device: str = "cuda"):
+def random_inputs(M: int, H: int, E: int, topk: int, seed: int = 0, device: str = "cuda",
+                  E_route: Optional[int] = None, shared: bool = False):
     """BF16 tokens ~N(0,1), topk distinct experts per token uniformly at
-    random, routing weights = softmax of N(0,1) logits over the picks."""
+    random over E_route experts (default E; an expert-parallel shard keeps
+    only the ids below E, the others are dropped by the layer), routing
+    weights = softmax of N(0,1) logits over the picks. shared: the last of
+    the topk columns is the shared expert E - 1 with weight 1 (the routed
+    picks are drawn over the other experts)."""
     import torch
     g = torch.Generator().manual_seed(seed)
     x = torch.randn(M, H, generator=g).to(torch.bfloat16)
-    ids = torch.argsort(torch.rand(M, E, generator=g), dim=1)[:, :topk].to(torch.int32)
-    w = torch.softmax(torch.randn(M, topk, generator=g), dim=1)
+    k = topk - 1 if shared else topk
+    span = E_route or (E - 1 if shared else E)
+    ids = torch.argsort(torch.rand(M, span, generator=g), dim=1)[:, :k].to(torch.int32)
+    w = torch.softmax(torch.randn(M, k, generator=g), dim=1)
+    if shared:
+        ids = torch.cat([ids, torch.full((M, 1), E - 1, dtype=torch.int32)], 1)
+        w = torch.cat([w, torch.ones(M, 1)], 1)
     return x.to(device), ids.contiguous().to(device), w.contiguous().to(device)
 
 
@@ -175,7 +188,8 @@ def _pairs(a: _Graph, b: _Graph, pairs, replays, flush, stream):
 def tune_geometry(H: int, Ip: int, E: int, topk: int, a16: bool, tokens: Sequence[int],
                   candidates: Sequence[int] = CANDIDATES, pairs: int = 31, replays: int = 16,
                   seed: int = 0, device: str = "cuda", log=print,
-                  buckets: Optional[Sequence[int]] = None) -> List[dict]:
+                  buckets: Optional[Sequence[int]] = None, E_route: Optional[int] = None,
+                  shared: bool = False) -> List[dict]:
     """Measure at each token count of `tokens` and record the result for the
     matching entry of `buckets` (the row's max_tokens; default: the token
     count itself), as the pages measure a real decode row per bucket."""
@@ -189,7 +203,7 @@ def tune_geometry(H: int, Ip: int, E: int, topk: int, a16: bool, tokens: Sequenc
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     rows = []
     for M, bucket in zip(tokens, buckets):
-        x, ids, w = random_inputs(M, H, E, topk, seed + M, device)
+        x, ids, w = random_inputs(M, H, E, topk, seed + M, device, E_route, shared)
         default = fused_moe_workspace_layout(M, H, Ip, E, topk, a16)["block_m"]
         base = _Graph(layer, x, ids, w, default, stream)
         twin = _Graph(layer, x, ids, w, default, stream)
@@ -233,11 +247,15 @@ def main(argv: Optional[Sequence[str]] = None) -> None:
     ap.add_argument("--candidates", type=int, nargs="+", default=list(CANDIDATES))
     ap.add_argument("--pairs", type=int, default=31)
     ap.add_argument("--replays", type=int, default=16)
+    ap.add_argument("--E-route", type=int, default=None,
+                    help="experts the routing draws from (expert-parallel shard: the global count)")
+    ap.add_argument("--shared", action="store_true",
+                    help="the last routing column is the shared expert E-1 (weight 1)")
     ap.add_argument("--out", required=True)
     ap.add_argument("--append", action="store_true", help="keep the rows already in --out")
     a = ap.parse_args(argv)
     rows = tune_geometry(a.H, a.Ip, a.E, a.topk, a.a16, a.tokens, a.candidates, a.pairs,
-                         a.replays, buckets=a.buckets)
+                         a.replays, buckets=a.buckets, E_route=a.E_route, shared=a.shared)
     if a.append:
         import os
         if os.path.exists(a.out):

@@ -112,6 +112,14 @@ def test_shipped_rows_by_geometry():
     assert list(draft) == [3] and draft[3][-1] == (1024, 32)
     backbone = shipped_block_m_rows(5120, 640, 384, False)
     assert [bm for _, bm in backbone[6]] == [16] * 8
-    assert shipped_block_m_rows(5120, 2304, 96, False) == {}     # not tuned
+    # expert-parallel shard (96 local experts of 384, routing over all 384)
+    ep = shipped_block_m_rows(5120, 2304, 96, False)
+    assert list(ep) == [6] and ep[6][-1] == (16384, 128)
+    assert dict(ep[6])[32] == 32 and dict(ep[6])[2048] == 64
+    # a16w4: 384 top-6, and 385 top-7 with the shared expert as expert 384
+    a16 = shipped_block_m_rows(5120, 768, 384, True)
+    assert list(a16) == [6] and dict(a16[6])[1024] == 32 and dict(a16[6])[4096] == 128
+    assert list(shipped_block_m_rows(5120, 768, 385, True)) == [7]
+    assert shipped_block_m_rows(4096, 640, 384, False) == {}     # not tuned
     lay = types.SimpleNamespace(block_m_table=[], _bm_by_topk=draft)
     assert MoeLayer.block_m_for(lay, 640, 3) == 32 and MoeLayer.block_m_for(lay, 320, 3) == 16
