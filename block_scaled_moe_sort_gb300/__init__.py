@@ -23,6 +23,7 @@ __all__ = [
     "fused_moe_a8w4", "fused_moe_a16w4", "MoeLayer", "HEADER", "declared_functions",
     "moe_profile_enable", "moe_profile_collect", "PROFILE_SLOTS", "fused_moe_a8w4_noalloc",
     "moe_noalloc_status", "fused_moe_gated", "shared_expert_pieces", "with_shared_expert",
+    "moe_prepack_weights_a16w4", "moe_dequant_a16w4",
 ]
 
 HEADER = os.path.join(_build.ROOT, "include", "moe_mx.h")
@@ -60,6 +61,10 @@ _SIGS = {
     "moe_prepack_weights_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p,
                                         _c_void_p]),
     "moe_prepack_scales_mx": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p, _c_void_p]),
+    "moe_prepack_weights_a16w4": (_c_int, [_c_void_p, _c_int, _c_int, _c_int, _c_void_p,
+                                           _c_void_p]),
+    "moe_dequant_a16w4": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
+                                   _c_void_p]),
     "fused_moe_workspace_bytes": (_c_size_t, [_c_int] * 6),
     "fused_moe_workspace_layout": (_c_int, [_c_int] * 6 + [ctypes.POINTER(MoeWsLayout)]),
     "fused_moe_a8w4": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
@@ -229,8 +234,7 @@ def moe_quant_act_mx(x: torch.Tensor, stream=None):
     return q, s
 
 
-def moe_prepack_weights_mx(w: torch.Tensor, stream=None) -> torch.Tensor:
-    """Row-major packed E2M1 codes [E, N, K/2] -> 8 KB weight tiles."""
+def _prepack_weights(fn: str, w: torch.Tensor, stream) -> torch.Tensor:
     assert w.dtype == torch.uint8 and w.dim() == 3
     E, N, KH = w.shape
     K = KH * 2
@@ -238,8 +242,28 @@ def moe_prepack_weights_mx(w: torch.Tensor, stream=None) -> torch.Tensor:
     if nbytes == 0:
         raise ValueError("unsupported weight shape (N and K must be multiples of 128)")
     out = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
-    _check("moe_prepack_weights_mx", lib().moe_prepack_weights_mx(_ptr(w), E, N, K, _ptr(out),
-                                                                  _stream(stream)))
+    _check(fn, getattr(lib(), fn)(_ptr(w), E, N, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def moe_prepack_weights_mx(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """Row-major packed E2M1 codes [E, N, K/2] -> 8 KB weight tiles (a8w4)."""
+    return _prepack_weights("moe_prepack_weights_mx", w, stream)
+
+
+def moe_prepack_weights_a16w4(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """Row-major packed E2M1 codes [E, N, K/2] -> the a16w4 weight tiles
+    (the same tiles, each 32-bit word in the a16w4 bit order)."""
+    return _prepack_weights("moe_prepack_weights_a16w4", w, stream)
+
+
+def moe_dequant_a16w4(w_packed: torch.Tensor, scale_packed: torch.Tensor, E: int, N: int, K: int,
+                      stream=None) -> torch.Tensor:
+    """Diagnostic: the a16w4 GEMMs' dequantisation of prepacked experts ->
+    BF16 [E, N, K]."""
+    out = torch.empty(E, N, K, dtype=torch.bfloat16, device=w_packed.device)
+    _check("moe_dequant_a16w4", lib().moe_dequant_a16w4(_ptr(w_packed), _ptr(scale_packed), E, N,
+                                                        K, _ptr(out), _stream(stream)))
     return out
 
 
@@ -317,8 +341,9 @@ def fused_moe_a8w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_pac
 def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
                     w2_scale_packed, E, Ip, out=None, ws=None, stream=None,
                     block_m: int = 0) -> torch.Tensor:
-    """BF16-activation x MXFP4-weight fused MoE on prepacked weights; returns
-    BF16 [M, H]. block_m 0 = the library's route block rule."""
+    """BF16-activation x MXFP4-weight fused MoE on weights prepacked by
+    moe_prepack_weights_a16w4; returns BF16 [M, H]. block_m 0 = the
+    library's route block rule."""
     return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
                   w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m)
 
@@ -495,8 +520,9 @@ class MoeLayer:
             self._bm_by_topk = shipped_block_m_rows(self.H, self.Ip, self.E, a16)
             block_m_table = None
         self.block_m_table = sorted(block_m_table) if block_m_table else []
-        self.w1 = moe_prepack_weights_mx(w1.to(device).contiguous())
-        self.w2 = moe_prepack_weights_mx(w2.to(device).contiguous())
+        prepack = moe_prepack_weights_a16w4 if a16 else moe_prepack_weights_mx
+        self.w1 = prepack(w1.to(device).contiguous())
+        self.w2 = prepack(w2.to(device).contiguous())
         self.w1_scale = moe_prepack_scales_mx(w1_scale.to(device).contiguous())
         self.w2_scale = moe_prepack_scales_mx(w2_scale.to(device).contiguous())
 

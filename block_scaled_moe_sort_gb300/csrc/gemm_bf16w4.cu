@@ -20,9 +20,11 @@
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps
 // 2..5 epilogue (TMEM lane quadrant = warp % 4), warps 6.. converters (4 or
 // 8; quadrant = warp % 4, with 8 warps each converts half of the stage's K).
-// A converter thread decodes its row's FP4 pairs through a 256-entry table of
-// BF16 pairs kept once per lane in shared memory (conflict-free lookups),
-// multiplies by the block scale and stores 32 TMEM columns at a time.
+// A converter thread turns its row's FP4 pairs into BF16 pairs with
+// rotations and masks (the a16w4 weight prepack stores every word in the bit
+// order that makes this work, dequant_a16.cuh), multiplies by the block
+// scale and stores 32 TMEM columns at a time; no lookup table, so shared
+// memory bandwidth stays with the TMA and the MMA's B operand.
 // Pipeline stage = 128 K-elements: one prepacked 8 KB weight tile, fetched by
 // TMA with the 64-byte swizzle (conflict-free row reads), its 512-byte scale
 // atom, and two 128-byte swizzle atoms of BF16 activations.
@@ -35,6 +37,7 @@
 #include "moe_internal.h"
 #include "sm100_ptx.cuh"
 #include "gemm_tiles.cuh"
+#include "dequant_a16.cuh"
 #include "timeline.cuh"
 
 MOE_TL_DEFINE(moe_tl_dump_bf16)
@@ -114,11 +117,10 @@ struct Cfg16 {
   static constexpr int kAccBufs = BN <= 128 ? 2 : 1;
   static constexpr int kAccCol0 = kASlots * kACols;
   static constexpr int kTmemCols = pow2_cols(kAccCol0 + kAccBufs * BN);
-  static constexpr int kLutWords = 256 * 32;
   static constexpr int kEpiFloats = 32 * (64 + 4);
   static constexpr int kRouteBytes = BN * 8;                   // per-tile route info
   static constexpr int kSmem =
-      1024 + kStages * kStageBytes + kLutWords * 4 + kEpiFloats * 4 + kRouteBytes;
+      1024 + kStages * kStageBytes + kEpiFloats * 4 + kRouteBytes;
   static constexpr uint32_t kTxBytes = kRawBytes + kSfBytes + kBBytes;
   // per SM: 228 KB, of which 1 KB is reserved per CTA; the static shared
   // variables (barriers, the local route layout) take up to kStaticSmem
@@ -126,33 +128,6 @@ struct Cfg16 {
   static_assert(kAccCol0 + kAccBufs * BN <= kTmemCols && kTmemCols * kCtasPerSm <= 512,
                 "TMEM budget");
 };
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
-  __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
-  __nv_bfloat162 z = __hmul2(x, y);
-  return *reinterpret_cast<uint32_t*>(&z);
-}
-
-// BF16 bit pattern of one E2M1 code: magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6
-// (exponent field 126 + e for e = 1..3, the subnormal code 1 is 0.5 = 0x3F00),
-// sign from bit 3.
-__device__ __forceinline__ uint32_t e2m1_bf16_bits(uint32_t c) {
-  const uint32_t e = (c >> 1) & 3, m = c & 1;
-  const uint32_t mag = e == 0 ? (m ? 0x3F00u : 0u) : (((126u + e) << 7) | (m << 6));
-  return mag | ((c & 8u) << 12);
-}
-
-__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t s) {
-  const uint32_t h = s == 0 ? 0x0040u : (s << 7);   // 2^(s-127) as BF16 (s=0: subnormal)
-  return h | (h << 16);
-}
 
 using Seq16 = TileSeq<Bf16Args>;          // producer: loads each tile's expert
 using Seq16R = TileSeq<Bf16Args, false>;  // other roles
@@ -166,8 +141,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   // 1024-byte aligned base, derived by pointer arithmetic so that the
   // compiler keeps every access below in the shared state space
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + C::kStages * C::kStageBytes);  // [256][32]
-  float* epi = reinterpret_cast<float*>(lut + C::kLutWords);
+  float* epi = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   int* s_tok = reinterpret_cast<int*>(epi + C::kEpiFloats);      // [BN] token / -1 pad
   float* s_w = reinterpret_cast<float*>(s_tok + BN);              // [BN] routing weight
   __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
@@ -205,13 +179,6 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     fence_mbar_init();
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmX);
-  }
-  // FP4 pair table: entry b holds the BF16 patterns of codes b & 15 (low
-  // half) and b >> 4 (high half), replicated once per lane so that every
-  // lane reads its own bank.
-  for (int i = threadIdx.x; i < C::kLutWords; i += blockDim.x) {
-    const uint32_t b = static_cast<uint32_t>(i) >> 5;
-    lut[i] = e2m1_bf16_bits(b & 15u) | (e2m1_bf16_bits(b >> 4) << 16);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, C::kTmemCols);
@@ -428,7 +395,6 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     const int h0 = C::kConvWarps == 8 ? (warp - 6) >> 2 : 0;
     const int swz = (r >> 1) & 3;                        // 64-byte swizzle of row r
     const int sf_off = sf_atom_off(r, 0);                // its 4 scale bytes
-    const uint32_t* lut_lane = lut + lane;
     const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     int stage = 0;
     uint32_t phase = 0;
@@ -473,26 +439,32 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         const uint8_t* raw = stage_ptr(stage) + C::kBBytes + r * 64;
         const uint32_t sfw =
             *reinterpret_cast<const uint32_t*>(stage_ptr(stage) + C::kBBytes + C::kRawBytes + sf_off);
+        auto convert = [&](auto any_scale) {
+          constexpr bool kAny = decltype(any_scale)::value;
+          const uint32_t tsc = sfw + 0x7E7E7E7Eu;         // s + 126 per byte (fast form)
 #pragma unroll
-        for (int hh = 0; hh < kHalves; ++hh) {
-          const int h = h0 + hh;                         // 64-element half of the stage
-          uint32_t out[32];
+          for (int hh = 0; hh < kHalves; ++hh) {
+            const int h = h0 + hh;                       // 64-element half of the stage
+            uint32_t out[32];
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {               // 32 elements = one scale block
-            const int c = 2 * h + cc;
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ swz) << 4));
-            const uint32_t sc = e8m0_bf16x2((sfw >> (8 * c)) & 0xFF);
-            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+            for (int cc = 0; cc < 2; ++cc) {             // 32 elements = one scale block
+              const int c = 2 * h + cc;
+              const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ swz) << 4));
+              uint32_t pairs[16];
+              if constexpr (kAny)
+                a16_dequant_block_any(v, (sfw >> (8 * c)) & 0xFFu, pairs);
+              else
+                a16_dequant_block(v, a16_scale_pair(tsc, c), pairs);
 #pragma unroll
-            for (int wi = 0; wi < 4; ++wi)
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                const uint32_t idx = prmt(words[wi], 0u, 0x4440u | b);
-                out[cc * 16 + wi * 4 + b] = bf16x2_mul(lut_lane[idx * 32], sc);
-              }
+              for (int i = 0; i < 16; ++i) out[cc * 16 + i] = pairs[i];
+            }
+            tmem_st_32x32b_x32(t_row + slot * kACols + h * 32, out);
           }
-          tmem_st_32x32b_x32(t_row + slot * kACols + h * 32, out);
-        }
+        };
+        if (__any_sync(0xffffffffu, a16_big_scales(sfw) != 0u))
+          convert(std::true_type{});
+        else
+          convert(std::false_type{});
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

@@ -34,7 +34,9 @@ cudaError_t launch_router_topk(const float* logits, int M, int E, int ld, int to
                                cudaStream_t s);
 
 cudaError_t launch_prepack_weights(const uint8_t* w, int E, int N, int K, uint8_t* out,
-                                   cudaStream_t s);
+                                   bool a16, cudaStream_t s);
+cudaError_t launch_dequant_a16w4(const uint8_t* w, const uint8_t* sf, int E, int N, int K,
+                                 void* out, cudaStream_t s);
 cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uint8_t* out,
                                   cudaStream_t s);
 

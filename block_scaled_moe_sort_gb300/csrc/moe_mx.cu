@@ -327,8 +327,28 @@ moe_status_t moe_prepack_weights_mx(const uint8_t* w, int E, int N, int K, uint8
   if (E <= 0 || N <= 0 || K <= 0 || !w || !out || w == out) return MOE_ERR_INVALID_ARG;
   if (N % 128 || K % 128) return MOE_ERR_UNSUPPORTED;
   if (!aligned(w) || !aligned(out)) return MOE_ERR_ALIGNMENT;
-  return from_cuda(launch_prepack_weights(w, E, N, K, out,
+  return from_cuda(launch_prepack_weights(w, E, N, K, out, false,
                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_prepack_weights_a16w4(const uint8_t* w, int E, int N, int K, uint8_t* out,
+                                       moe_stream_t stream) {
+  if (E <= 0 || N <= 0 || K <= 0 || !w || !out || w == out) return MOE_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(w) || !aligned(out)) return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_prepack_weights(w, E, N, K, out, true,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_dequant_a16w4(const uint8_t* w_packed, const uint8_t* scale_packed, int E, int N,
+                               int K, void* out_bf16, moe_stream_t stream) {
+  if (E <= 0 || N <= 0 || K <= 0 || !w_packed || !scale_packed || !out_bf16)
+    return MOE_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(w_packed) || !aligned(scale_packed) || !aligned(out_bf16))
+    return MOE_ERR_ALIGNMENT;
+  return from_cuda(launch_dequant_a16w4(w_packed, scale_packed, E, N, K, out_bf16,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_prepacked_scale_bytes(int E, int N, int K) {

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include "common.cuh"
 #include "moe_internal.h"
+#include "dequant_a16.cuh"
 #include "router_warp.cuh"
 #include "sm100_ptx.cuh"
 #include "timeline.cuh"
@@ -372,7 +373,9 @@ __global__ void __launch_bounds__(256) prepack_scales_kernel(const uint8_t* __re
 }
 
 // Row-major packed codes [E][N][K/2] -> tiles [E][N/128][K/128][128][64 B],
-// one 16-byte chunk per thread.
+// one 16-byte chunk per thread; kA16: every 32-bit word in the a16w4 bit
+// order (dequant_a16.cuh).
+template <bool kA16>
 __global__ void __launch_bounds__(256) prepack_weights_kernel(const uint8_t* __restrict__ w,
                                                               int E, int N, int K,
                                                               uint8_t* __restrict__ out) {
@@ -389,7 +392,45 @@ __global__ void __launch_bounds__(256) prepack_weights_kernel(const uint8_t* __r
     const int nb = static_cast<int>(a % nb_n);
     const int e = static_cast<int>(a / nb_n);
     const int64_t src = (static_cast<int64_t>(e) * N + nb * 128 + r) * (K / 2) + kb * 64 + c * 16;
-    reinterpret_cast<uint4*>(out)[o] = *reinterpret_cast<const uint4*>(w + src);
+    uint4 v = *reinterpret_cast<const uint4*>(w + src);
+    if constexpr (kA16) {
+      v.x = a16_permute_word(v.x);
+      v.y = a16_permute_word(v.y);
+      v.z = a16_permute_word(v.z);
+      v.w = a16_permute_word(v.w);
+    }
+    reinterpret_cast<uint4*>(out)[o] = v;
+  }
+}
+
+// Diagnostic: the a16w4 converter's dequantisation of whole prepacked
+// experts (tiles and scale atoms as the GEMMs read them) to BF16 [E][N][K],
+// one 32-element block per thread.
+__global__ void __launch_bounds__(256) dequant_a16w4_kernel(const uint8_t* __restrict__ w,
+                                                            const uint8_t* __restrict__ sf,
+                                                            int E, int N, int K,
+                                                            __nv_bfloat16* __restrict__ out) {
+  const int64_t total = static_cast<int64_t>(E) * N * (K / 32);
+  const int nb_k = K / 128;
+  for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
+       o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int blk = static_cast<int>(o % (K / 32));
+    const int64_t row = o / (K / 32);             // e * N + n
+    const int n = static_cast<int>(row % N);
+    const int64_t e = row / N;
+    const int kb = blk >> 2, c = blk & 3, r = n & 127;
+    const int64_t tile = (e * (N / 128) + n / 128) * nb_k + kb;
+    const uint4 v = *reinterpret_cast<const uint4*>(w + tile * 8192 + r * 64 + c * 16);
+    const uint32_t s = sf[tile * 512 + sf_atom_off(r, c)];
+    uint32_t pairs[16];
+    if (a16_big_scales(s) != 0u)
+      a16_dequant_block_any(v, s, pairs);
+    else
+      a16_dequant_block(v, a16_scale_pair(s + 0x7Eu, 0), pairs);
+    uint4* dst = reinterpret_cast<uint4*>(out + row * K + blk * 32);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      dst[q] = make_uint4(pairs[4 * q], pairs[4 * q + 1], pairs[4 * q + 2], pairs[4 * q + 3]);
   }
 }
 
@@ -513,10 +554,23 @@ cudaError_t launch_prepack_scales(const uint8_t* scale, int E, int N, int K, uin
 }
 
 cudaError_t launch_prepack_weights(const uint8_t* w, int E, int N, int K, uint8_t* out,
-                                   cudaStream_t s) {
+                                   bool a16, cudaStream_t s) {
   const int64_t total = static_cast<int64_t>(E) * N * (K / 2) / 16;
   if (total == 0) return cudaSuccess;
-  prepack_weights_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, s>>>(w, E, N, K, out);
+  const int grid = grid_for(total, 256, 152 * 16);
+  if (a16)
+    prepack_weights_kernel<true><<<grid, 256, 0, s>>>(w, E, N, K, out);
+  else
+    prepack_weights_kernel<false><<<grid, 256, 0, s>>>(w, E, N, K, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_a16w4(const uint8_t* w, const uint8_t* sf, int E, int N, int K,
+                                 void* out, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(E) * N * (K / 32);
+  if (total == 0) return cudaSuccess;
+  dequant_a16w4_kernel<<<grid_for(total, 256, 152 * 16), 256, 0, s>>>(
+      w, sf, E, N, K, static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 

@@ -5,10 +5,11 @@
 // measured runtime, times the call including gating; the weights are the
 // softmax over the picks, as in the pages' synthetic routing).
 //
-// Lane l holds logits l, l+32, ... as order-preserving integer keys, so each
-// of the topk rounds picks the next expert with two warp reductions (largest
-// key, then lowest expert holding it); lane j keeps pick j. Used by the
-// standalone gating kernel and by the decode front kernel of the gated call.
+// Lane l holds logits l, l+32, ... as order-preserving integer keys and
+// keeps its three largest; each of the topk rounds picks the largest head
+// key of the warp (the lowest expert among equal keys); lane j keeps pick j.
+// Used by the standalone gating kernel and by the decode front kernel of the
+// gated call.
 #pragma once
 #include <cstdint>
 
@@ -36,30 +37,71 @@ __device__ __forceinline__ void router_load(const float* row, int E, int lane,
   }
 }
 
-// Selects the topk experts of the keys in v (consumed). Lane j < topk gets
-// pick j: its expert in *expert and its routing weight in *weight.
+// This lane's kCache largest keys in (key descending, slot ascending) order,
+// among the keys that come after (lk, ls) in that order (all keys for
+// lk = ~0u, ls = -1); empty entries have key 0.
+constexpr int kRouterCache = 3;
 template <int SLOTS>
-__device__ __forceinline__ void router_select(uint32_t (&v)[SLOTS], int topk, int lane,
+__device__ __forceinline__ void router_lane_top(const uint32_t (&v)[SLOTS], uint32_t lk, int ls,
+                                                uint32_t (&hk)[kRouterCache],
+                                                int (&hs)[kRouterCache]) {
+#pragma unroll
+  for (int c = 0; c < kRouterCache; ++c) { hk[c] = 0u; hs[c] = 0; }
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    const uint32_t k = v[i];
+    if (!(k < lk || (k == lk && i > ls))) continue;
+    // insertion after the entries >= k (an equal key of a lower slot stays first)
+    if (k > hk[kRouterCache - 1]) {
+#pragma unroll
+      for (int c = kRouterCache - 1; c > 0; --c) {
+        if (k > hk[c - 1]) { hk[c] = hk[c - 1]; hs[c] = hs[c - 1]; }
+        else if (k > hk[c]) { hk[c] = k; hs[c] = i; }
+      }
+      if (k > hk[0]) { hk[0] = k; hs[0] = i; }
+    }
+  }
+}
+
+// Selects the topk experts of the keys in v. Lane j < topk gets pick j: its
+// expert in *expert and its routing weight in *weight.
+// Each lane first keeps its three largest keys; every round takes the warp's
+// largest head key (one reduction; a second one, over expert ids, only when
+// several lanes hold that key) and the winning lane moves to its next key,
+// rescanning its slots after the keys it has given (rare: a lane holding
+// more than three of the picks).
+template <int SLOTS>
+__device__ __forceinline__ void router_select(const uint32_t (&v)[SLOTS], int topk, int lane,
                                               int* expert, float* weight) {
-  uint32_t mine = 0;   // lane j: key of pick j
+  uint32_t hk[kRouterCache];
+  int hs[kRouterCache];
+  router_lane_top<SLOTS>(v, ~0u, -1, hk, hs);
+  int left = kRouterCache;     // cached entries of this lane not yet given
+  uint32_t mine = 0;           // lane j: key of pick j
   int mine_e = 0;
   for (int j = 0; j < topk; ++j) {
-    // this lane's best remaining expert (slots in ascending e: ties keep the lower)
-    uint32_t bk = 0;
-    int be = 0;
-#pragma unroll
-    for (int i = 0; i < SLOTS; ++i)
-      if (v[i] > bk) { bk = v[i]; be = i * 32 + lane; }
-    // warp arg-max in two reductions: the largest key, then the lowest
-    // expert among the lanes that hold it
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-    const int win = static_cast<int>(
-        __reduce_min_sync(0xffffffffu, bk == kmax ? static_cast<uint32_t>(be) : 0xffffffffu));
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, hk[0]);
+    const uint32_t holders = __ballot_sync(0xffffffffu, hk[0] == kmax);
+    int win;
+    if (__popc(holders) == 1) {
+      const int wl = __ffs(holders) - 1;
+      win = __shfl_sync(0xffffffffu, hs[0], wl) * 32 + wl;
+    } else {
+      // equal largest keys in several lanes: the lowest expert
+      win = static_cast<int>(__reduce_min_sync(
+          0xffffffffu, hk[0] == kmax ? static_cast<uint32_t>(hs[0] * 32 + lane) : 0xffffffffu));
+    }
     if (lane == j) { mine = kmax; mine_e = win; }
     if ((win & 31) == lane) {
+      const uint32_t lk = hk[0];
+      const int ls = hs[0];
 #pragma unroll
-      for (int i = 0; i < SLOTS; ++i)
-        if (i == (win >> 5)) v[i] = 0u;
+      for (int c = 0; c + 1 < kRouterCache; ++c) { hk[c] = hk[c + 1]; hs[c] = hs[c + 1]; }
+      hk[kRouterCache - 1] = 0u;
+      if (--left == 0) {
+        router_lane_top<SLOTS>(v, lk, ls, hk, hs);
+        left = kRouterCache;
+      }
     }
   }
   // softmax over the picks, shifted by the largest (pick 0)

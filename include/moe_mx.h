@@ -149,6 +149,30 @@ size_t moe_prepacked_weight_bytes(int E, int N, int K);
 moe_status_t moe_prepack_weights_mx(const uint8_t* w, int E, int N, int K, uint8_t* out,
                                     moe_stream_t stream);
 
+/* moe_prepack_weights_a16w4: the weight prepack of the a16w4 calls (the
+ * weights fused_moe_a16w4* take). The same tiles as moe_prepack_weights_mx,
+ * and within every 32-bit word of eight E2M1 codes (code j in bits
+ * 4j..4j+3, bit 3 the sign) the bits are moved so that the GEMM turns each
+ * pair of codes into two BF16 values with a rotation and a mask: pair 0 =
+ * w & P, pair 1 = rotr(w, 6) & P, pair 2 = rotr(w, 12) & P, pair 3 =
+ * (rotr(w, 2) & PA) | (rotr(w, 10) & PB), with P = 0x81C081C0, PA =
+ * 0x81808180, PB = 0x00400040; each BF16 half then holds its code's
+ * mantissa, exponent and sign at bits 6, 7-8 and 15 (the E2M1 value times
+ * 2^-126). Same size, limits and errors as moe_prepack_weights_mx. */
+moe_status_t moe_prepack_weights_a16w4(const uint8_t* w, int E, int N, int K, uint8_t* out,
+                                       moe_stream_t stream);
+
+/* moe_dequant_a16w4 (diagnostic): the a16w4 GEMMs' dequantisation of whole
+ * experts, run by the same device routine: w_packed from
+ * moe_prepack_weights_a16w4, scale_packed from moe_prepack_scales_mx, out
+ * BF16 [E, N, K] (device), element (e, n, k) = E2M1 code times 2^(s - 127)
+ * of its block (OCP Microscaling Formats v1.0: MXFP4), exact wherever the
+ * product is a BF16 number; products past the BF16 range are infinities,
+ * and the NaN scale (255) gives infinities (NaN for the zero codes).
+ * Limits and errors as moe_prepack_weights_mx. */
+moe_status_t moe_dequant_a16w4(const uint8_t* w_packed, const uint8_t* scale_packed, int E, int N,
+                               int K, void* out_bf16, moe_stream_t stream);
+
 /* ---------------------------------------------------- weight scale prepack
  * The GEMMs read weight scales in 512-byte atoms. moe_prepack_scales_mx
  * converts row-major scales [E, N, K/32] into [E][N/128][K/128][512]: in the
@@ -216,7 +240,9 @@ moe_status_t fused_moe_a8w4(const void* x, const int32_t* topk_ids, const float*
                             void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* fused_moe_a16w4: as fused_moe_a8w4 with BF16 activations (no activation
- * quantisation) and a BF16 intermediate. Same arguments and limits. */
+ * quantisation) and a BF16 intermediate; w1 / w2 come from
+ * moe_prepack_weights_a16w4 (not moe_prepack_weights_mx). Otherwise the same
+ * arguments and limits. */
 moe_status_t fused_moe_a16w4(const void* x, const int32_t* topk_ids,
                              const float* topk_weights, int M, int H, int topk,
                              const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2,

@@ -17,7 +17,8 @@ def L():
 def test_header_declares_the_entry_points():
     names = m.declared_functions()
     for want in ["moe_sort", "moe_quant_act_mx", "fused_moe_a8w4", "fused_moe_a16w4", "moe_router_topk",
-                 "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "moe_status_string"]:
+                 "moe_prepack_scales_mx", "fused_moe_workspace_bytes", "moe_status_string",
+                 "moe_prepack_weights_a16w4", "moe_dequant_a16w4"]:
         assert want in names
 
 
@@ -95,6 +96,15 @@ def test_sort_and_quant_reject_bad_arguments(L):
     assert L.moe_quant_act_mx(FAKE + 8, 4, 128, 128, FAKE, FAKE, None) == 4
     assert L.moe_prepack_scales_mx(FAKE, 2, 100, 256, FAKE, None) == 2
     assert L.moe_prepacked_scale_bytes(2, 256, 512) == 2 * 256 * 16
+    for fn in ("moe_prepack_weights_mx", "moe_prepack_weights_a16w4"):
+        f = getattr(L, fn)
+        assert f(FAKE, 2, 100, 256, FAKE + 0x1000, None) == 2          # N % 128
+        assert f(FAKE, 2, 128, 256, FAKE, None) == 1                   # out aliases w
+        assert f(FAKE + 8, 2, 128, 256, FAKE + 0x1000, None) == 4
+        assert f(None, 2, 128, 256, FAKE, None) == 1
+    assert L.moe_dequant_a16w4(FAKE, FAKE, 1, 128, 200, FAKE, None) == 2     # K % 128
+    assert L.moe_dequant_a16w4(FAKE, None, 1, 128, 256, FAKE, None) == 1
+    assert L.moe_dequant_a16w4(FAKE, FAKE, 1, 128, 256, FAKE + 4, None) == 4
 
 
 def test_device_status_decoding(L):

@@ -100,3 +100,35 @@ def test_prepack_scale_layout(cuda_lib, E, N, K):
     want = np.zeros(E * N * K // 32, dtype=np.uint8)
     want[off.reshape(-1)] = s.reshape(-1)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("E,N,K", [(2, 256, 256), (1, 128, 5120)])
+def test_a16w4_dequant_exact(cuda_lib, E, N, K):
+    # The a16w4 GEMMs' weight dequantisation (a16w4 prepack + the converter's
+    # rotations, masks and scale multiplication, run by the same device
+    # routine) against the OCP MXFP4 definition: every byte of codes and
+    # every finite E8M0 scale 0..254, exact wherever the product is a BF16
+    # number and infinite past the BF16 range; the NaN scale 255 gives no
+    # finite value for a nonzero code.
+    g = np.random.default_rng(E * N + K)
+    w = g.integers(0, 256, size=(E, N, K // 2), dtype=np.uint8)
+    w.reshape(-1)[:256] = np.arange(256, dtype=np.uint8)
+    s = (np.arange(E * N * (K // 32)) % 256).astype(np.uint8).reshape(E, N, K // 32)
+    s = np.ascontiguousarray(s[:, g.permutation(N), :])
+    wp = m.moe_prepack_weights_a16w4(torch.from_numpy(w).cuda())
+    sp = m.moe_prepack_scales_mx(torch.from_numpy(s).cuda())
+    got = m.moe_dequant_a16w4(wp, sp, E, N, K).cpu().to(torch.float64).numpy()
+    finite_scale = np.repeat(s != 255, 32, axis=-1)
+    want = mx.bf16_round(np.where(finite_scale, mx.dequant_mxfp4(w, np.where(s == 255, 0, s)), 0))
+    assert np.array_equal(got[finite_scale], want[finite_scale])
+    # the sign of zero as well (code 8 is -0)
+    assert np.array_equal(np.signbit(got[finite_scale]), np.signbit(want[finite_scale]))
+    codes = mx.unpack_e2m1(w)
+    nan_scale = ~finite_scale & ((codes & 7) != 0)
+    assert not np.isfinite(got[nan_scale]).any()
+    # the a8w4 prepack is the plain tile copy; the a16w4 one moves bits only
+    # inside each 32-bit word (same bytes per tile row, same popcount per word)
+    plain = m.moe_prepack_weights_mx(torch.from_numpy(w).cuda()).cpu().numpy().view(np.uint32)
+    a16 = wp.cpu().numpy().view(np.uint32)
+    pc = lambda a: np.unpackbits(a.view(np.uint8)).reshape(-1, 32).sum(axis=1)
+    assert np.array_equal(pc(plain), pc(a16)) and not np.array_equal(plain, a16)
