@@ -16,9 +16,8 @@
 // the code's exponent field e, so a normal code 2^(e-1) (1 + m/2) becomes
 // 2^(e-127) (1 + m/2), and the subnormal code m/2 becomes the BF16 subnormal
 // (m/2) 2^-126. One BF16 multiplication by 2^(s - 1) then applies the block
-// scale exactly (s <= 128; a row whose k-block has a larger exponent takes
-// two multiplications, a path the warp takes only when one of its rows needs
-// it).
+// scale exactly (s <= 128; for a larger exponent a second multiplication
+// follows, a path the warp takes only when one of its rows needs it).
 // Canonical order: code j of a word in bits 4j..4j+3, bit 3 the sign, bits
 // 2-1 the exponent, bit 0 the mantissa (byte b holds codes 2b and 2b+1).
 #pragma once
@@ -79,22 +78,23 @@ __device__ __forceinline__ uint32_t a16_scale_pair(uint32_t t, int c) {
   return b * 0x00800080u;
 }
 
-// The 16 BF16 pairs of one block for any scale byte s: scaled to the E2M1
-// value (2^126), then by 2^(s-127); products past the BF16 range become
-// infinities, and the NaN scale s = 255 gives infinities (NaN for the zero
-// codes).
-__device__ __forceinline__ void a16_dequant_block_any(const uint4 v, uint32_t s,
-                                                      uint32_t (&out)[16]) {
-  uint32_t t[16];
-  a16_tiny_block(v, t);
-  const uint32_t up = 0x7E807E80u;
-  const uint32_t h = s << 7;
-  const uint32_t sc = h | (h << 16);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) out[i] = a16_bf16x2_mul(a16_bf16x2_mul(t[i], up), sc);
+// For a scale byte above 128 the block is converted with the pair of 128
+// (2^127: the tiny values times 2^127 stay at most 12) and then multiplied
+// by this second pair, 2^(s - 128); s = 255, the NaN scale, gives
+// infinities (NaN for the zero codes). For s <= 128 the pair is 1.
+__device__ __forceinline__ uint32_t a16_big_pair(uint32_t s) {
+  const uint32_t h = s == 255u ? 0x7F80u : ((s > 128u ? s : 128u) - 1u) << 7;
+  return h * 0x00010001u;
 }
 
-// Fast form for scale bytes <= 128: one multiplication by the pair sc.
+// Pair of the first multiplication for any scale byte: 2^(min(s, 128) - 1).
+__device__ __forceinline__ uint32_t a16_first_pair(uint32_t s) {
+  return ((s < 128u ? s : 128u) + 126u) * 0x00800080u;
+}
+
+// The 16 BF16 pairs (K order) of one block from its four a16w4 words: the
+// tiny values times the pair sc (a16_scale_pair, or a16_first_pair and then
+// a16_big_pair for a scale byte above 128).
 __device__ __forceinline__ void a16_dequant_block(const uint4 v, uint32_t sc, uint32_t (&out)[16]) {
   uint32_t t[16];
   a16_tiny_block(v, t);

@@ -439,32 +439,31 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         const uint8_t* raw = stage_ptr(stage) + C::kBBytes + r * 64;
         const uint32_t sfw =
             *reinterpret_cast<const uint32_t*>(stage_ptr(stage) + C::kBBytes + C::kRawBytes + sf_off);
-        auto convert = [&](auto any_scale) {
-          constexpr bool kAny = decltype(any_scale)::value;
-          const uint32_t tsc = sfw + 0x7E7E7E7Eu;         // s + 126 per byte (fast form)
+        // a scale byte above 128 in one of the warp's rows (never for real
+        // weights): the warp converts this k-block with a second multiplication
+        const bool big = __any_sync(0xffffffffu, a16_big_scales(sfw) != 0u);
+        const uint32_t tsc = sfw + 0x7E7E7E7Eu;           // s + 126 per byte when !big
 #pragma unroll
-          for (int hh = 0; hh < kHalves; ++hh) {
-            const int h = h0 + hh;                       // 64-element half of the stage
-            uint32_t out[32];
+        for (int hh = 0; hh < kHalves; ++hh) {
+          const int h = h0 + hh;                           // 64-element half of the stage
+          uint32_t out[32];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {             // 32 elements = one scale block
-              const int c = 2 * h + cc;
-              const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ swz) << 4));
-              uint32_t pairs[16];
-              if constexpr (kAny)
-                a16_dequant_block_any(v, (sfw >> (8 * c)) & 0xFFu, pairs);
-              else
-                a16_dequant_block(v, a16_scale_pair(tsc, c), pairs);
+          for (int cc = 0; cc < 2; ++cc) {                 // 32 elements = one scale block
+            const int c = 2 * h + cc;
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + ((c ^ swz) << 4));
+            const uint32_t sb = (sfw >> (8 * c)) & 0xFFu;
+            uint32_t pairs[16];
+            a16_dequant_block(v, big ? a16_first_pair(sb) : a16_scale_pair(tsc, c), pairs);
+            if (big) {
+              const uint32_t sc2 = a16_big_pair(sb);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) out[cc * 16 + i] = pairs[i];
+              for (int i = 0; i < 16; ++i) pairs[i] = a16_bf16x2_mul(pairs[i], sc2);
             }
-            tmem_st_32x32b_x32(t_row + slot * kACols + h * 32, out);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) out[cc * 16 + i] = pairs[i];
           }
-        };
-        if (__any_sync(0xffffffffu, a16_big_scales(sfw) != 0u))
-          convert(std::true_type{});
-        else
-          convert(std::false_type{});
+          tmem_st_32x32b_x32(t_row + slot * kACols + h * 32, out);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

@@ -423,10 +423,13 @@ __global__ void __launch_bounds__(256) dequant_a16w4_kernel(const uint8_t* __res
     const uint4 v = *reinterpret_cast<const uint4*>(w + tile * 8192 + r * 64 + c * 16);
     const uint32_t s = sf[tile * 512 + sf_atom_off(r, c)];
     uint32_t pairs[16];
-    if (a16_big_scales(s) != 0u)
-      a16_dequant_block_any(v, s, pairs);
-    else
-      a16_dequant_block(v, a16_scale_pair(s + 0x7Eu, 0), pairs);
+    const bool big = a16_big_scales(s) != 0u;
+    a16_dequant_block(v, big ? a16_first_pair(s) : a16_scale_pair(s + 0x7Eu, 0), pairs);
+    if (big) {
+      const uint32_t sc2 = a16_big_pair(s);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pairs[i] = a16_bf16x2_mul(pairs[i], sc2);
+    }
     uint4* dst = reinterpret_cast<uint4*>(out + row * K + blk * 32);
 #pragma unroll
     for (int q = 0; q < 4; ++q)

@@ -6,8 +6,8 @@
 // softmax over the picks, as in the pages' synthetic routing).
 //
 // Lane l holds logits l, l+32, ... as order-preserving integer keys and
-// keeps its three largest; each of the topk rounds picks the largest head
-// key of the warp (the lowest expert among equal keys); lane j keeps pick j.
+// keeps its two largest; each of the topk rounds picks the largest head key
+// of the warp (the lowest expert among equal keys); lane j keeps pick j.
 // Used by the standalone gating kernel and by the decode front kernel of the
 // gated call.
 #pragma once
@@ -19,8 +19,9 @@ namespace moe {
 // both zeros map to the key of +0 so that they tie, and key 0 is below every
 // finite value (it marks absent and already picked experts).
 __device__ __forceinline__ uint32_t logit_key(float f) {
-  const uint32_t u = f == 0.f ? 0u : __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(f + 0.0f);                    // -0 + +0 = +0
+  const uint32_t neg = static_cast<uint32_t>(static_cast<int32_t>(u) >> 31);
+  return u ^ (neg | 0x80000000u);   // negative: all bits flipped; else the sign bit set
 }
 __device__ __forceinline__ float key_logit(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
@@ -37,70 +38,62 @@ __device__ __forceinline__ void router_load(const float* row, int E, int lane,
   }
 }
 
-// This lane's kCache largest keys in (key descending, slot ascending) order,
-// among the keys that come after (lk, ls) in that order (all keys for
-// lk = ~0u, ls = -1); empty entries have key 0.
-constexpr int kRouterCache = 3;
-template <int SLOTS>
-__device__ __forceinline__ void router_lane_top(const uint32_t (&v)[SLOTS], uint32_t lk, int ls,
-                                                uint32_t (&hk)[kRouterCache],
-                                                int (&hs)[kRouterCache]) {
-#pragma unroll
-  for (int c = 0; c < kRouterCache; ++c) { hk[c] = 0u; hs[c] = 0; }
-#pragma unroll
-  for (int i = 0; i < SLOTS; ++i) {
-    const uint32_t k = v[i];
-    if (!(k < lk || (k == lk && i > ls))) continue;
-    // insertion after the entries >= k (an equal key of a lower slot stays first)
-    if (k > hk[kRouterCache - 1]) {
-#pragma unroll
-      for (int c = kRouterCache - 1; c > 0; --c) {
-        if (k > hk[c - 1]) { hk[c] = hk[c - 1]; hs[c] = hs[c - 1]; }
-        else if (k > hk[c]) { hk[c] = k; hs[c] = i; }
-      }
-      if (k > hk[0]) { hk[0] = k; hs[0] = i; }
-    }
-  }
+// Keeps (h0, s0) >= (h1, s1), the two largest (key, slot) seen in (key
+// descending, slot ascending) order: slots come in ascending order, so an
+// equal key never displaces an earlier one.
+__device__ __forceinline__ void router_insert2(uint32_t k, int i, uint32_t& h0, int& s0,
+                                               uint32_t& h1, int& s1) {
+  const bool c0 = k > h0, c1 = k > h1;
+  h1 = c0 ? h0 : (c1 ? k : h1);
+  s1 = c0 ? s0 : (c1 ? i : s1);
+  h0 = c0 ? k : h0;
+  s0 = c0 ? i : s0;
 }
 
 // Selects the topk experts of the keys in v. Lane j < topk gets pick j: its
 // expert in *expert and its routing weight in *weight.
-// Each lane first keeps its three largest keys; every round takes the warp's
+// Each lane first keeps its two largest keys; every round takes the warp's
 // largest head key (one reduction; a second one, over expert ids, only when
-// several lanes hold that key) and the winning lane moves to its next key,
-// rescanning its slots after the keys it has given (rare: a lane holding
-// more than three of the picks).
+// several lanes hold that key) and the winning lane moves to its second key,
+// or, having given both, rescans its slots for the two that follow the last
+// one it gave.
 template <int SLOTS>
 __device__ __forceinline__ void router_select(const uint32_t (&v)[SLOTS], int topk, int lane,
                                               int* expert, float* weight) {
-  uint32_t hk[kRouterCache];
-  int hs[kRouterCache];
-  router_lane_top<SLOTS>(v, ~0u, -1, hk, hs);
-  int left = kRouterCache;     // cached entries of this lane not yet given
+  uint32_t h0 = 0u, h1 = 0u;
+  int s0 = 0, s1 = 0;
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) router_insert2(v[i], i, h0, s0, h1, s1);
+  bool second = false;         // this lane has given one of its two cached keys
   uint32_t mine = 0;           // lane j: key of pick j
   int mine_e = 0;
   for (int j = 0; j < topk; ++j) {
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, hk[0]);
-    const uint32_t holders = __ballot_sync(0xffffffffu, hk[0] == kmax);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, h0);
+    const uint32_t holders = __ballot_sync(0xffffffffu, h0 == kmax);
     int win;
     if (__popc(holders) == 1) {
       const int wl = __ffs(holders) - 1;
-      win = __shfl_sync(0xffffffffu, hs[0], wl) * 32 + wl;
+      win = __shfl_sync(0xffffffffu, s0, wl) * 32 + wl;
     } else {
       // equal largest keys in several lanes: the lowest expert
       win = static_cast<int>(__reduce_min_sync(
-          0xffffffffu, hk[0] == kmax ? static_cast<uint32_t>(hs[0] * 32 + lane) : 0xffffffffu));
+          0xffffffffu, h0 == kmax ? static_cast<uint32_t>(s0 * 32 + lane) : 0xffffffffu));
     }
     if (lane == j) { mine = kmax; mine_e = win; }
     if ((win & 31) == lane) {
-      const uint32_t lk = hk[0];
-      const int ls = hs[0];
+      if (!second) {
+        h0 = h1; s0 = s1;
+        second = true;
+      } else {
+        // both cached keys given: the two that follow (h0, s0) in the order
+        const uint32_t lk = h0;
+        const int ls = s0;
+        h0 = h1 = 0u;
+        s0 = s1 = 0;
 #pragma unroll
-      for (int c = 0; c + 1 < kRouterCache; ++c) { hk[c] = hk[c + 1]; hs[c] = hs[c + 1]; }
-      hk[kRouterCache - 1] = 0u;
-      if (--left == 0) {
-        router_lane_top<SLOTS>(v, lk, ls, hk, hs);
-        left = kRouterCache;
+        for (int i = 0; i < SLOTS; ++i)
+          if (v[i] < lk || (v[i] == lk && i > ls)) router_insert2(v[i], i, h0, s0, h1, s1);
+        second = false;
       }
     }
   }
