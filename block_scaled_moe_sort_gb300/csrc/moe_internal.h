@@ -107,7 +107,7 @@ struct GemmPlan {
 };
 // tcgen05 block-scaled grouped GEMM, a8w4, stage 1 or 2.
 cudaError_t prepare_gemm_mx(int stage, const GemmArgs& a, GemmPlan* plan);
-// tcgen05 BF16 x (MXFP4 dequantised in shared memory) grouped GEMM, a16w4.
+// tcgen05 BF16 x (MXFP4 dequantised into TMEM) grouped GEMM, a16w4.
 cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& a, GemmPlan* plan);
 cudaError_t launch_gemm(const GemmPlan& plan, cudaStream_t s);
 
