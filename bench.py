@@ -52,7 +52,9 @@ import torch  # noqa: E402
 import moe_inputs as mi  # noqa: E402
 
 # decode sweep of each workload's geometry (the pages' token buckets)
-SWEEP = {"backbone": mi.TOKENS["backbone"], "draft": mi.TOKENS["draft"], "ep": mi.TOKENS["ep"],
+# the draft sweep follows its tuned decode rows (M=5 is the pages' draft row)
+SWEEP = {"backbone": mi.TOKENS["backbone"], "draft": [5, 10, 20, 40, 80, 160, 320, 640],
+         "ep": mi.TOKENS["ep"],
          "a16w4_384": mi.TOKENS["a16w4"], "a16w4_385": mi.TOKENS["a16w4"], "zipf": []}
 L2_FLUSH_BYTES = 256 << 20
 

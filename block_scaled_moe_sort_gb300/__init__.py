@@ -45,6 +45,11 @@ class MoeWsLayout(ctypes.Structure):
                 ("split_cnt_off", _c_int64), ("total_bytes", _c_int64)]
 
 
+class MoeCallConfig(ctypes.Structure):
+    _fields_ = [("block_m", ctypes.c_int32), ("prefetch1", ctypes.c_int32),
+                ("prefetch2", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_c_int]),
     "moe_sort_max_padded": (_c_int64, [_c_int, _c_int, _c_int, _c_int]),
@@ -81,6 +86,14 @@ _SIGS = {
     "fused_moe_a16w4_bm": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
                                     _c_void_p, _c_void_p, _c_size_t, _c_int, _c_void_p]),
+    "fused_moe_a8w4_cfg": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                    _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
+                                    _c_void_p, _c_void_p, _c_size_t,
+                                    ctypes.POINTER(MoeCallConfig), _c_void_p]),
+    "fused_moe_a16w4_cfg": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
+                                     _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_int, _c_int,
+                                     _c_void_p, _c_void_p, _c_size_t,
+                                     ctypes.POINTER(MoeCallConfig), _c_void_p]),
     "moe_decode_device_status": (_c_int, [ctypes.c_int32]),
     "moe_debug_wait_selftest": (_c_int, [_c_void_p, _c_int, _c_void_p]),
     "fused_moe_a8w4_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int,
@@ -306,7 +319,7 @@ def fused_moe_workspace_layout(M: int, H: int, Ip: int, E: int, topk: int, a16: 
 
 
 def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
-           E, Ip, out=None, ws=None, stream=None, block_m=0):
+           E, Ip, out=None, ws=None, stream=None, block_m=0, prefetch=None):
     M, H = x.shape
     topk = topk_ids.shape[1]
     a16 = fn_name == "fused_moe_a16w4"
@@ -321,7 +334,11 @@ def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
     args = [_ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, H, topk, _ptr(w1),
             _ptr(w1_scale_packed), _ptr(w2), _ptr(w2_scale_packed), E, Ip, _ptr(out), _ptr(ws),
             ws.numel()]
-    if block_m:
+    if prefetch and any(prefetch):
+        fn_name = fn_name + "_cfg"
+        cfg = MoeCallConfig(int(block_m), int(prefetch[0]), int(prefetch[1]), 0)
+        args.append(ctypes.byref(cfg))
+    elif block_m:
         fn_name = fn_name + "_bm"
         args.append(block_m)
     code = getattr(lib(), fn_name)(*args, _stream(stream))
@@ -331,21 +348,23 @@ def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
 
 def fused_moe_a8w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
                    w2_scale_packed, E, Ip, out=None, ws=None, stream=None,
-                   block_m: int = 0) -> torch.Tensor:
+                   block_m: int = 0, prefetch=None) -> torch.Tensor:
     """FP8-activation x MXFP4-weight fused MoE on prepacked weights; returns
-    BF16 [M, H]. block_m 0 = the library's route block rule."""
+    BF16 [M, H]. block_m 0 = the library's route block rule; prefetch
+    (stage-1, stage-2 weight L2 prefetch lead in weight tiles, 0 = default)
+    goes through fused_moe_a8w4_cfg."""
     return _fused("fused_moe_a8w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
-                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m)
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch)
 
 
 def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
                     w2_scale_packed, E, Ip, out=None, ws=None, stream=None,
-                    block_m: int = 0) -> torch.Tensor:
+                    block_m: int = 0, prefetch=None) -> torch.Tensor:
     """BF16-activation x MXFP4-weight fused MoE on weights prepacked by
     moe_prepack_weights_a16w4; returns BF16 [M, H]. block_m 0 = the
-    library's route block rule."""
+    library's route block rule; prefetch as for fused_moe_a8w4."""
     return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
-                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m)
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch)
 
 
 def fused_moe_gated(x, router_logits, topk, w1_packed, w1_scale_packed, w2_packed,
@@ -470,12 +489,16 @@ def with_shared_expert(w1, w1_scale, w2, w2_scale, shared):
 
 def shipped_block_m_rows(H: int, Ip: int, E: int, a16: bool) -> dict:
     """The shipped GB300 tuning rows of one geometry: topk -> sorted
-    [(max_tokens, block_m), ...] (empty for a geometry that was not tuned)."""
+    [(max_tokens, block_m[, prefetch1, prefetch2]), ...] (the prefetch leads
+    where a tuned row sets them; empty for a geometry that was not tuned)."""
     from . import tune
     by_topk = {}
     for r in tune.read_table(tune.PACKAGED_TABLE):
         if (r["H"], r["Ip"], r["E"], r["a16"]) == (H, Ip, E, int(a16)):
-            by_topk.setdefault(r["topk"], []).append((r["max_tokens"], r["block_m"]))
+            row = (r["max_tokens"], r["block_m"])
+            if r["prefetch1"] or r["prefetch2"]:
+                row += (r["prefetch1"], r["prefetch2"])
+            by_topk.setdefault(r["topk"], []).append(row)
     for rows in by_topk.values():
         rows.sort()
     return by_topk
@@ -484,11 +507,12 @@ def shipped_block_m_rows(H: int, Ip: int, E: int, a16: bool) -> dict:
 class MoeLayer:
     """Device-resident MXFP4 expert weights with prepacked scales.
 
-    block_m_table: rows (max_tokens, block_m) sorted by max_tokens (see
-    block_scaled_moe_sort_gb300.tune): a call with M tokens uses the route
-    block of the first row with M <= max_tokens; beyond the last row, or
-    without a table, the library's own rule applies. "gb300" takes the rows
-    of this geometry from the table shipped with the package.
+    block_m_table: rows (max_tokens, block_m[, prefetch1, prefetch2]) sorted
+    by max_tokens (see block_scaled_moe_sort_gb300.tune): a call with M
+    tokens uses the route block (and weight prefetch leads) of the first row
+    with M <= max_tokens; beyond the last row, or without a table, the
+    library's own choices apply. "gb300" takes the rows of this geometry
+    from the table shipped with the package.
 
     shared_expert: (w1, w1_scale, w2, w2_scale) of one separate shared
     expert that every token uses with weight 1 (the shared-first layouts of
@@ -544,16 +568,26 @@ class MoeLayer:
                                shared_id=self.shared_id, out=out, ws=ws, stream=stream,
                                n_shared=max(self.n_shared, 1))
 
-    def block_m_for(self, M: int, topk: Optional[int] = None) -> int:
-        """Route block for an M-token call (0 = the library's rule)."""
+    def _row_for(self, M: int, topk: Optional[int]):
         table = self.block_m_table
         by_topk = getattr(self, "_bm_by_topk", None)
         if by_topk is not None:
             table = by_topk.get(topk, [])
-        for max_tokens, bm in table:
-            if M <= max_tokens:
-                return int(bm)
-        return 0
+        for row in table:
+            if M <= row[0]:
+                return row
+        return None
+
+    def block_m_for(self, M: int, topk: Optional[int] = None) -> int:
+        """Route block for an M-token call (0 = the library's rule)."""
+        row = MoeLayer._row_for(self, M, topk)
+        return int(row[1]) if row else 0
+
+    def prefetch_for(self, M: int, topk: Optional[int] = None):
+        """(stage-1, stage-2) weight prefetch leads for an M-token call
+        ((0, 0) = the library's defaults)."""
+        row = MoeLayer._row_for(self, M, topk)
+        return (int(row[2]), int(row[3])) if row and len(row) >= 4 else (0, 0)
 
     def workspace_bytes(self, M: int, topk: int) -> int:
         return fused_moe_workspace_bytes(M, self.H, self.Ip, self.E, topk, self.a16,
@@ -563,8 +597,11 @@ class MoeLayer:
         return fused_moe_workspace_layout(M, self.H, self.Ip, self.E, topk, self.a16,
                                           self.block_m_for(M, topk))
 
-    def __call__(self, x, topk_ids, topk_weights, out=None, ws=None, stream=None, block_m=None):
+    def __call__(self, x, topk_ids, topk_weights, out=None, ws=None, stream=None, block_m=None,
+                 prefetch=None):
         fn = fused_moe_a16w4 if self.a16 else fused_moe_a8w4
-        bm = self.block_m_for(x.shape[0], topk_ids.shape[1]) if block_m is None else block_m
+        M, k = x.shape[0], topk_ids.shape[1]
+        bm = self.block_m_for(M, k) if block_m is None else block_m
+        pf = self.prefetch_for(M, k) if prefetch is None else prefetch
         return fn(x, topk_ids, topk_weights, self.w1, self.w1_scale, self.w2, self.w2_scale,
-                  self.E, self.Ip, out=out, ws=ws, stream=stream, block_m=bm)
+                  self.E, self.Ip, out=out, ws=ws, stream=stream, block_m=bm, prefetch=pf)

@@ -83,6 +83,7 @@ struct Bf16Args {
   const uint8_t* sfa;          // weight scale atoms [E][N/128][K/128][512]
   __nv_bfloat16* inter;        // stage 1 out: BF16 [p_max, Ip]
   float* acc;                  // stage 2 out
+  int prefetch;                // weight L2 prefetch lead in k-blocks
   int32_t* status;
 };
 
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      constexpr int kPrefetch = 8;
+      const int kPrefetch = a.prefetch;   // per call; 8 by default
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed_mask = 0, armed_par = 0;   // stages armed, parity of their last arming
@@ -706,6 +707,8 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.w = stage == 1 ? g.w1 : g.w2;
   a.inter = static_cast<__nv_bfloat16*>(g.inter);
   a.acc = g.acc;
+  a.prefetch = stage == 1 ? (g.prefetch1 > 0 ? g.prefetch1 : 8)
+                         : (g.prefetch2 > 0 ? g.prefetch2 : 8);
   a.status = g.status;
   plan->grid = 0;
   if (a.num_blocks == 0) return cudaSuccess;

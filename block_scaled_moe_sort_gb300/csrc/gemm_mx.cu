@@ -83,6 +83,7 @@ struct MxArgs {
   uint8_t* inter;        // stage 1 out: E4M3 [p_max, Ip]
   uint8_t* inter_sf;     // stage 1 out: atoms [blocks][Ip/128][na][512]
   float* acc;            // stage 2 out: [M, H]
+  int prefetch;          // weight L2 prefetch lead in k-blocks
   int32_t* status;
   // stage-1 tail split (decode): FP32 partial sums [kSplitSlots][BN][128] and
   // arrival counters [kSplitSlots], zero at the start of the call
@@ -211,9 +212,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_x = policy_evict_last();    // routes: reused across n-tiles
-      // k-blocks the L2 prefetch runs ahead; stage-2 tiles (five k-blocks)
-      // do better with a shorter lead (measured: 8 vs 16 vs 32)
-      const int kPrefetch = a.stage == 2 ? 8 : 16;
+      // k-blocks the L2 prefetch runs ahead (per call; by default 16 in
+      // stage 1 and 8 in stage 2, whose five-k-block tiles do better with a
+      // shorter lead: measured 8 vs 16 vs 32)
+      const int kPrefetch = a.prefetch;
       constexpr uint32_t kWTile = kTileN * kTileK / 2;   // 8 KB
       int stage = 0;
       uint32_t phase = 0;
@@ -780,6 +782,8 @@ cudaError_t prepare_gemm_mx(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.inter = static_cast<uint8_t*>(g.inter);
   a.inter_sf = g.inter_sf;
   a.acc = g.acc;
+  a.prefetch = stage == 1 ? (g.prefetch1 > 0 ? g.prefetch1 : 16)
+                         : (g.prefetch2 > 0 ? g.prefetch2 : 8);
   a.status = g.status;
   a.split_part = g.split_part;
   a.split_cnt = g.split_cnt;

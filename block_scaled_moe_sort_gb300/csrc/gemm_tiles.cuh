@@ -63,7 +63,7 @@ __device__ __forceinline__ int local_block_layout(const int32_t* ids, int R, int
       router_load<16>(gate.logits + static_cast<int64_t>(t) * gate.ld, gate.E_route, lane, v);
       int e;
       float w;
-      router_select<16>(v, gate.topk_sel, lane, &e, &w);
+      router_select_rounds<16>(v, gate.topk_sel, lane, &e, &w);
       if (lane >= gate.topk_sel && lane < gate.topk_sel + gate.n_shared)
         e = gate.shared_id + lane - gate.topk_sel;
       if (lane < k) sid[t * k + lane] = e;

@@ -75,6 +75,7 @@ cudaError_t launch_finalize(const float* acc, int64_t n, void* out, cudaStream_t
 struct GemmArgs {
   bool a16;
   int M, H, Ip, E, topk, bm;
+  int prefetch1, prefetch2;  // weight L2 prefetch lead per stage in k-blocks (0 = default)
   int64_t p_max;
   const int32_t* topk_ids;   // the call's routing input (local layout at decode sizes)
   LocalGate gate;            // gated calls: router logits instead (topk_ids is then null)

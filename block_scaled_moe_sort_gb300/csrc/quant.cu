@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
       router_load<SLOTS>(a.logits + static_cast<int64_t>(tt) * a.ld, a.E_route, lane, v);
       int e;
       float w;
-      router_select<SLOTS>(v, a.topk_sel, lane, &e, &w);
+      router_select_rounds<SLOTS>(v, a.topk_sel, lane, &e, &w);
       if (lane >= a.topk_sel && lane < a.topk_sel + a.n_shared) {   // shared columns
         e = a.shared_id + lane - a.topk_sel;
         w = 1.f;

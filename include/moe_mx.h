@@ -190,7 +190,11 @@ moe_status_t moe_prepack_scales_mx(const uint8_t* scale, int E, int N, int K, ui
  * caller allocates it (device, 256-byte aligned) and may reuse it for any
  * later call with the same or a smaller shape. Contents need no
  * initialisation. Two calls in flight on different streams need different
- * workspaces.
+ * workspaces. Results are not bitwise reproducible from call to call: the
+ * routing-weighted sum (and, for small a8w4 calls, the split K ranges of the
+ * last stage-1 tiles) is added in FP32 by atomic reductions whose order
+ * varies; the sorted lists are deterministic, and so is the intermediate
+ * outside those split tiles.
  */
 typedef struct {
   int32_t block_m;       /* route block of both GEMMs (= sort block) */
@@ -271,6 +275,37 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
                                 const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
                                 void* out, void* ws, size_t ws_bytes, int block_m,
                                 moe_stream_t stream);
+
+/* ------------------------------------------------ per-call configuration
+ * The calls with every per-call tuning parameter the caller may set (the
+ * rows of a per-token-bucket tuning table; AITER #5609 "Add DeepSeek V4.1
+ * Flash TP4 gfx950 MoE tuning", Configuration: one configuration per
+ * geometry and token bucket). A zero field is the library's choice.
+ *   block_m    route block, as for the *_bm calls (0, 16, 32, 64, 128, 256);
+ *              the workspace is sized by fused_moe_workspace_bytes_bm with it
+ *   prefetch1  stage-1 weight L2 prefetch lead in 128-K weight tiles, 1..64
+ *              (default 16 for a8w4, 8 for a16w4)
+ *   prefetch2  the same for stage 2 (default 8)
+ *   reserved   must be 0 (MOE_ERR_INVALID_ARG otherwise)
+ * Out-of-range values give MOE_ERR_UNSUPPORTED. cfg NULL = all defaults.
+ * The result does not depend on the prefetch leads (they only move weight
+ * tiles into L2 earlier or later). */
+typedef struct {
+  int32_t block_m;
+  int32_t prefetch1;
+  int32_t prefetch2;
+  int32_t reserved;
+} moe_call_config_t;
+moe_status_t fused_moe_a8w4_cfg(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                                int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                                const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                                void* out, void* ws, size_t ws_bytes,
+                                const moe_call_config_t* cfg /* host */, moe_stream_t stream);
+moe_status_t fused_moe_a16w4_cfg(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                                 int M, int H, int topk, const uint8_t* w1, const uint8_t* w1_scale,
+                                 const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
+                                 void* out, void* ws, size_t ws_bytes,
+                                 const moe_call_config_t* cfg /* host */, moe_stream_t stream);
 
 /* ------------------------------------------------------- gated calls
  * fused_moe_a8w4_gated / fused_moe_a16w4_gated: the fused calls with the

@@ -107,6 +107,21 @@ def test_sort_and_quant_reject_bad_arguments(L):
     assert L.moe_dequant_a16w4(FAKE, FAKE, 1, 128, 256, FAKE + 4, None) == 4
 
 
+def test_call_config_checks(L):
+    import block_scaled_moe_sort_gb300 as mm
+    args = [FAKE, FAKE, FAKE, 4, 256, 2, FAKE, FAKE, FAKE, FAKE, 8, 128, FAKE, FAKE, 1 << 40]
+    for fn in ("fused_moe_a8w4_cfg", "fused_moe_a16w4_cfg"):
+        f = getattr(L, fn)
+        bad = mm.MoeCallConfig(0, 0, 0, 1)                  # reserved must be 0
+        assert f(*args, ctypes.byref(bad), None) == 1
+        far = mm.MoeCallConfig(0, 65, 0, 0)                 # lead past 64 tiles
+        assert f(*args, ctypes.byref(far), None) == 2
+        neg = mm.MoeCallConfig(0, 0, -1, 0)
+        assert f(*args, ctypes.byref(neg), None) == 2
+        odd = mm.MoeCallConfig(48, 0, 0, 0)                 # not a route block
+        assert f(*args, ctypes.byref(odd), None) == 2
+
+
 def test_device_status_decoding(L):
     assert L.moe_decode_device_status(0) == 0
     assert L.moe_decode_device_status(1) == 6

@@ -54,6 +54,30 @@ def test_explicit_block_m(cuda_lib, a16, bm):
     assert st["block_m"] == bm
 
 
+@pytest.mark.parametrize("a16", [False, True])
+@pytest.mark.parametrize("pf", [(1, 1), (64, 64), (4, 16)])
+def test_explicit_prefetch(cuda_lib, a16, pf):
+    # the second tuning knob (fused_moe_*_cfg): weight L2 prefetch leads at
+    # their extremes; they move weights into L2 earlier or later and must
+    # not change the result
+    shp = mi.small_shape(H=512, I=192, Ip=256, E=8, topk=3, E_route=10, a16=a16)
+    w = mi.make_weights(shp, 5)
+    layer = m.MoeLayer(w["w1"], w["w1_scale"], w["w2"], w["w2_scale"], a16=a16,
+                       block_m_table=[(1 << 30, 16, pf[0], pf[1])])
+    assert layer.prefetch_for(130, 3) == pf
+    case = mi.make_case("small", 130, shape=shp, weights=w)
+    compare(case, layer, a16)
+
+
+def test_explicit_prefetch_backbone(cuda_lib):
+    # the pages' backbone geometry at a decode bucket, sampled tokens
+    wts = __import__("moe_check").weights_for("backbone", 0)
+    layer = m.MoeLayer(wts["w1"], wts["w1_scale"], wts["w2"], wts["w2_scale"],
+                       block_m_table=[(1 << 30, 16, 32, 4)])
+    case = mi.make_case("backbone", 384, weights=wts)
+    print(compare(case, layer, False, tokens=sample_tokens(384, 8, 11)))
+
+
 def test_empty_experts_and_all_dropped_tokens(cuda_lib):
     shp = mi.small_shape(H=256, I=128, Ip=128, E=16, topk=2, E_route=64)
     w, layer = _small_layer(shp, 9)

@@ -67,7 +67,8 @@ def test_table_round_trip_and_geometry_filter(tmp_path):
     p = tmp_path / "t.csv"
     tune.write_table(rows, str(p))
     back = tune.read_table(str(p))
-    assert back == rows
+    assert [{k: r[k] for k in rows[0]} for r in back] == rows
+    assert all(r["prefetch1"] == 0 and r["prefetch2"] == 0 for r in back)   # knob unset
     assert tune.table_for(back, 5120, 640, 384, 6, False) == [(8, 16), (64, 32), (1024, 64)]
     assert tune.table_for(back, 5120, 640, 128, 3, False) == [(16, 16)]
     assert tune.table_for(back, 5120, 640, 384, 6, True) == []
@@ -111,7 +112,7 @@ def test_shipped_rows_by_geometry():
     draft = shipped_block_m_rows(5120, 640, 128, False)
     assert list(draft) == [3] and draft[3][-1] == (1024, 32)
     backbone = shipped_block_m_rows(5120, 640, 384, False)
-    assert [bm for _, bm in backbone[6]] == [16] * 8
+    assert [r[1] for r in backbone[6]] == [16] * 8
     # expert-parallel shard (96 local experts of 384, routing over all 384)
     ep = shipped_block_m_rows(5120, 2304, 96, False)
     assert list(ep) == [6] and ep[6][-1] == (16384, 128)
@@ -123,3 +124,23 @@ def test_shipped_rows_by_geometry():
     assert shipped_block_m_rows(4096, 640, 384, False) == {}     # not tuned
     lay = types.SimpleNamespace(block_m_table=[], _bm_by_topk=draft)
     assert MoeLayer.block_m_for(lay, 640, 3) == 32 and MoeLayer.block_m_for(lay, 320, 3) == 16
+
+
+def test_prefetch_knob_round_trip_and_lookup(tmp_path):
+    rows = [_row(64, 32), _row(1024, 64)]
+    rows[1].update(prefetch1=24, prefetch2=4, prefetch_gain=0.02, prefetch_wins=30)
+    p = tmp_path / "t.csv"
+    tune.write_table(rows, str(p))
+    back = tune.read_table(str(p))
+    assert back[0]["prefetch1"] == 0 and back[0]["prefetch2"] == 0
+    assert (back[1]["prefetch1"], back[1]["prefetch2"], back[1]["prefetch_wins"]) == (24, 4, 30)
+    # a table written before the knob existed reads with zeros
+    old = tmp_path / "old.csv"
+    old.write_text("H,Ip,E,topk,a16,max_tokens,block_m,default_block_m,median_gain,wins,pairs,"
+                   "control_gain,control_wins\n5120,640,384,6,0,8,16,16,0.0,0,31,0.0,15\n")
+    r = tune.read_table(str(old))[0]
+    assert (r["prefetch1"], r["prefetch2"], r["prefetch_gain"]) == (0, 0, 0.0)
+    lay = types.SimpleNamespace(block_m_table=[(64, 32), (1024, 64, 24, 4)])
+    assert MoeLayer.block_m_for(lay, 10) == 32 and MoeLayer.prefetch_for(lay, 10) == (0, 0)
+    assert MoeLayer.block_m_for(lay, 500) == 64 and MoeLayer.prefetch_for(lay, 500) == (24, 4)
+    assert MoeLayer.prefetch_for(lay, 5000) == (0, 0)
