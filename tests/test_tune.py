@@ -110,20 +110,27 @@ def test_layer_lookup_by_topk_for_shipped_rows():
 def test_shipped_rows_by_geometry():
     from block_scaled_moe_sort_gb300 import shipped_block_m_rows
     draft = shipped_block_m_rows(5120, 640, 128, False)
-    assert list(draft) == [3] and draft[3][-1] == (1024, 32)
+    # rows: (max_tokens, block_m[, prefetch1, prefetch2])
+    assert list(draft) == [3] and draft[3][-1][:2] == (1024, 32)
     backbone = shipped_block_m_rows(5120, 640, 384, False)
     assert [r[1] for r in backbone[6]] == [16] * 8
+    # the measured prefetch leads: short ones won at every decode bucket
+    assert all(len(r) == 4 and 1 <= r[2] <= 8 and 1 <= r[3] <= 8 for r in backbone[6])
+    bm = lambda rows: {r[0]: r[1] for r in rows}
     # expert-parallel shard (96 local experts of 384, routing over all 384)
     ep = shipped_block_m_rows(5120, 2304, 96, False)
-    assert list(ep) == [6] and ep[6][-1] == (16384, 128)
-    assert dict(ep[6])[32] == 32 and dict(ep[6])[2048] == 64
-    # a16w4: 384 top-6, and 385 top-7 with the shared expert as expert 384
+    assert list(ep) == [6] and ep[6][-1] == (16384, 128)          # prefill: defaults kept
+    assert bm(ep[6])[32] == 32 and bm(ep[6])[2048] == 64
+    # a16w4: 384 top-6, and 385 top-7 with the shared expert as expert 384;
+    # no prefetch lead passed the gate (the converters bound these calls)
     a16 = shipped_block_m_rows(5120, 768, 384, True)
-    assert list(a16) == [6] and dict(a16[6])[1024] == 32 and dict(a16[6])[4096] == 128
+    assert list(a16) == [6] and bm(a16[6])[1024] == 32 and bm(a16[6])[4096] == 128
+    assert all(len(r) == 2 for r in a16[6])
     assert list(shipped_block_m_rows(5120, 768, 385, True)) == [7]
     assert shipped_block_m_rows(4096, 640, 384, False) == {}     # not tuned
     lay = types.SimpleNamespace(block_m_table=[], _bm_by_topk=draft)
     assert MoeLayer.block_m_for(lay, 640, 3) == 32 and MoeLayer.block_m_for(lay, 320, 3) == 16
+    assert MoeLayer.prefetch_for(lay, 640, 3) == draft[3][-1][2:]
 
 
 def test_prefetch_knob_round_trip_and_lookup(tmp_path):
