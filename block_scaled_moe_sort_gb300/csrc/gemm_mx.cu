@@ -212,9 +212,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_x = policy_evict_last();    // routes: reused across n-tiles
-      // k-blocks the L2 prefetch runs ahead (per call; by default 16 in
-      // stage 1 and 8 in stage 2, whose five-k-block tiles do better with a
-      // shorter lead: measured 8 vs 16 vs 32)
+      // k-blocks the L2 prefetch runs ahead (per call; the defaults are set
+      // where the launch is prepared)
       const int kPrefetch = a.prefetch;
       constexpr uint32_t kWTile = kTileN * kTileK / 2;   // 8 KB
       int stage = 0;
@@ -782,8 +781,12 @@ cudaError_t prepare_gemm_mx(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.inter = static_cast<uint8_t*>(g.inter);
   a.inter_sf = g.inter_sf;
   a.acc = g.acc;
-  a.prefetch = stage == 1 ? (g.prefetch1 > 0 ? g.prefetch1 : 16)
-                         : (g.prefetch2 > 0 ? g.prefetch2 : 8);
+  // default leads 4 and 2 tiles: the tuned decode rows of every a8w4
+  // geometry settled on them (1-10 % faster than 16 / 8) and they are also
+  // the fastest measured at prefill (M=4096-16384: 0.5-1.3 %; 32 or 64 tiles
+  // are slower)
+  a.prefetch = stage == 1 ? (g.prefetch1 > 0 ? g.prefetch1 : 4)
+                         : (g.prefetch2 > 0 ? g.prefetch2 : 2);
   a.status = g.status;
   a.split_part = g.split_part;
   a.split_cnt = g.split_cnt;

@@ -52,7 +52,7 @@ FIELDS = ["H", "Ip", "E", "topk", "a16", "max_tokens", "block_m", "default_block
           "prefetch1", "prefetch2", "prefetch_gain", "prefetch_wins"]
 CANDIDATES = (16, 32, 64, 128)
 # (stage-1, stage-2) weight L2 prefetch leads tried against the defaults
-# (a8w4 16/8, a16w4 8/8), in 128-K weight tiles
+# (a8w4 4/2, a16w4 8/8), in 128-K weight tiles
 PREFETCH_CANDIDATES = ((8, 8), (24, 8), (32, 8), (16, 4), (16, 16), (4, 4))
 
 

@@ -284,8 +284,8 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
  *   block_m    route block, as for the *_bm calls (0, 16, 32, 64, 128, 256);
  *              the workspace is sized by fused_moe_workspace_bytes_bm with it
  *   prefetch1  stage-1 weight L2 prefetch lead in 128-K weight tiles, 1..64
- *              (default 16 for a8w4, 8 for a16w4)
- *   prefetch2  the same for stage 2 (default 8)
+ *              (default a8w4 4, a16w4 8)
+ *   prefetch2  the same for stage 2 (default a8w4 2, a16w4 8)
  *   reserved   must be 0 (MOE_ERR_INVALID_ARG otherwise)
  * Out-of-range values give MOE_ERR_UNSUPPORTED. cfg NULL = all defaults.
  * The result does not depend on the prefetch leads (they only move weight
