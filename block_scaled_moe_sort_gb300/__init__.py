@@ -47,7 +47,7 @@ class MoeWsLayout(ctypes.Structure):
 
 class MoeCallConfig(ctypes.Structure):
     _fields_ = [("block_m", ctypes.c_int32), ("prefetch1", ctypes.c_int32),
-                ("prefetch2", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("prefetch2", ctypes.c_int32), ("split", ctypes.c_int32)]
 
 
 _SIGS = {
@@ -319,7 +319,7 @@ def fused_moe_workspace_layout(M: int, H: int, Ip: int, E: int, topk: int, a16: 
 
 
 def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale_packed,
-           E, Ip, out=None, ws=None, stream=None, block_m=0, prefetch=None):
+           E, Ip, out=None, ws=None, stream=None, block_m=0, prefetch=None, split=0):
     M, H = x.shape
     topk = topk_ids.shape[1]
     a16 = fn_name == "fused_moe_a16w4"
@@ -334,9 +334,10 @@ def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
     args = [_ptr(x), _ptr(topk_ids), _ptr(topk_weights), M, H, topk, _ptr(w1),
             _ptr(w1_scale_packed), _ptr(w2), _ptr(w2_scale_packed), E, Ip, _ptr(out), _ptr(ws),
             ws.numel()]
-    if prefetch and any(prefetch):
+    if (prefetch and any(prefetch)) or split:
         fn_name = fn_name + "_cfg"
-        cfg = MoeCallConfig(int(block_m), int(prefetch[0]), int(prefetch[1]), 0)
+        pf = prefetch or (0, 0)
+        cfg = MoeCallConfig(int(block_m), int(pf[0]), int(pf[1]), int(split))
         args.append(ctypes.byref(cfg))
     elif block_m:
         fn_name = fn_name + "_bm"
@@ -348,23 +349,25 @@ def _fused(fn_name, x, topk_ids, topk_weights, w1, w1_scale_packed, w2, w2_scale
 
 def fused_moe_a8w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
                    w2_scale_packed, E, Ip, out=None, ws=None, stream=None,
-                   block_m: int = 0, prefetch=None) -> torch.Tensor:
+                   block_m: int = 0, prefetch=None, split: int = 0) -> torch.Tensor:
     """FP8-activation x MXFP4-weight fused MoE on prepacked weights; returns
     BF16 [M, H]. block_m 0 = the library's route block rule; prefetch
     (stage-1, stage-2 weight L2 prefetch lead in weight tiles, 0 = default)
-    goes through fused_moe_a8w4_cfg."""
+    and split (the GEMMs' split walk: 0 = the library's rule, 1 = always,
+    2 = never) go through fused_moe_a8w4_cfg."""
     return _fused("fused_moe_a8w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
-                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch)
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch, split)
 
 
 def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_packed,
                     w2_scale_packed, E, Ip, out=None, ws=None, stream=None,
-                    block_m: int = 0, prefetch=None) -> torch.Tensor:
+                    block_m: int = 0, prefetch=None, split: int = 0) -> torch.Tensor:
     """BF16-activation x MXFP4-weight fused MoE on weights prepacked by
     moe_prepack_weights_a16w4; returns BF16 [M, H]. block_m 0 = the
-    library's route block rule; prefetch as for fused_moe_a8w4."""
+    library's route block rule; prefetch as for fused_moe_a8w4; split 0 or 2
+    (there is no split walk in the a16w4 GEMMs)."""
     return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
-                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch)
+                  w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch, split)
 
 
 def fused_moe_gated(x, router_logits, topk, w1_packed, w1_scale_packed, w2_packed,
@@ -489,15 +492,18 @@ def with_shared_expert(w1, w1_scale, w2, w2_scale, shared):
 
 def shipped_block_m_rows(H: int, Ip: int, E: int, a16: bool) -> dict:
     """The shipped GB300 tuning rows of one geometry: topk -> sorted
-    [(max_tokens, block_m[, prefetch1, prefetch2]), ...] (the prefetch leads
-    where a tuned row sets them; empty for a geometry that was not tuned)."""
+    [(max_tokens, block_m[, prefetch1, prefetch2[, split]]), ...] (the
+    prefetch leads and the split walk where a tuned row sets them; empty for
+    a geometry that was not tuned)."""
     from . import tune
     by_topk = {}
     for r in tune.read_table(tune.PACKAGED_TABLE):
         if (r["H"], r["Ip"], r["E"], r["a16"]) == (H, Ip, E, int(a16)):
             row = (r["max_tokens"], r["block_m"])
-            if r["prefetch1"] or r["prefetch2"]:
+            if r["prefetch1"] or r["prefetch2"] or r["split"]:
                 row += (r["prefetch1"], r["prefetch2"])
+            if r["split"]:
+                row += (r["split"],)
             by_topk.setdefault(r["topk"], []).append(row)
     for rows in by_topk.values():
         rows.sort()
@@ -507,9 +513,9 @@ def shipped_block_m_rows(H: int, Ip: int, E: int, a16: bool) -> dict:
 class MoeLayer:
     """Device-resident MXFP4 expert weights with prepacked scales.
 
-    block_m_table: rows (max_tokens, block_m[, prefetch1, prefetch2]) sorted
-    by max_tokens (see block_scaled_moe_sort_gb300.tune): a call with M
-    tokens uses the route block (and weight prefetch leads) of the first row
+    block_m_table: rows (max_tokens, block_m[, prefetch1, prefetch2[, split]])
+    sorted by max_tokens (see block_scaled_moe_sort_gb300.tune): a call with M
+    tokens uses the route block (weight prefetch leads, split walk) of the first row
     with M <= max_tokens; beyond the last row, or without a table, the
     library's own choices apply. "gb300" takes the rows of this geometry
     from the table shipped with the package.
@@ -589,6 +595,11 @@ class MoeLayer:
         row = MoeLayer._row_for(self, M, topk)
         return (int(row[2]), int(row[3])) if row and len(row) >= 4 else (0, 0)
 
+    def split_for(self, M: int, topk: Optional[int] = None) -> int:
+        """Split walk for an M-token call (0 = the library's rule)."""
+        row = MoeLayer._row_for(self, M, topk)
+        return int(row[4]) if row and len(row) >= 5 else 0
+
     def workspace_bytes(self, M: int, topk: int) -> int:
         return fused_moe_workspace_bytes(M, self.H, self.Ip, self.E, topk, self.a16,
                                          self.block_m_for(M, topk))
@@ -598,10 +609,12 @@ class MoeLayer:
                                           self.block_m_for(M, topk))
 
     def __call__(self, x, topk_ids, topk_weights, out=None, ws=None, stream=None, block_m=None,
-                 prefetch=None):
+                 prefetch=None, split=None):
         fn = fused_moe_a16w4 if self.a16 else fused_moe_a8w4
         M, k = x.shape[0], topk_ids.shape[1]
         bm = self.block_m_for(M, k) if block_m is None else block_m
         pf = self.prefetch_for(M, k) if prefetch is None else prefetch
+        sp = self.split_for(M, k) if split is None else split
         return fn(x, topk_ids, topk_weights, self.w1, self.w1_scale, self.w2, self.w2_scale,
-                  self.E, self.Ip, out=out, ws=ws, stream=stream, block_m=bm, prefetch=pf)
+                  self.E, self.Ip, out=out, ws=ws, stream=stream, block_m=bm, prefetch=pf,
+                  split=sp)

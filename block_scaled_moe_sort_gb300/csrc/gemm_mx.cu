@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     moe_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const MxArgs a) {
   using C = Cfg<BN>;
-  // SPLIT: stage 1 with the tail split (SplitSeq units, partial-sum epilogue)
+  // SPLIT: the split walk (SplitSeq units; stage 1 finishes split tiles
+  // through the partial-sum slots)
   // the producer's walk loads each tile's expert; the other roles' walks do not
   using Seq = typename std::conditional<SPLIT, SplitSeq<MxArgs>, TileSeq<MxArgs>>::type;
   using SeqR = typename std::conditional<SPLIT, SplitSeq<MxArgs, false>,
@@ -472,13 +473,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       const uint32_t d_tmem = tmem + ab * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
       constexpr int kChunk = BN < 32 ? BN : 32;
-      // Tail split: a K range of a split tile adds its partial sums to the
-      // tile's slot (feature row fastest: a warp adds 128 contiguous bytes),
-      // releases the accumulator and counts itself in; the range that arrives
-      // last reads the complete sums back from L2 and runs the epilogue.
+      // Split walk, stage 1: a part of a split tile adds its partial sums to
+      // the tile's slot (feature row fastest: a warp adds 128 contiguous
+      // bytes), releases the accumulator and counts itself in; the part that
+      // arrives last reads the complete sums back from L2 and runs the
+      // epilogue. (Stage 2 adds every part to the accumulator directly.)
       float* part = nullptr;
       if constexpr (SPLIT) {
-        if (seq.slot >= 0) {
+        if (seq.slot >= 0 && a.stage == 1) {
           part = a.split_part + static_cast<int64_t>(seq.slot) * BN * 128;
           for (int c0 = 0; c0 < BN; c0 += kChunk) {
             float v[32];
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
           if (lane == 0) mbar_arrive(&acc_empty[ab]);
           __threadfence();
           named_bar_sync(1, 128);
-          if (et == 0) split_last = atomicAdd(a.split_cnt + seq.slot, 1) == seq.S - 1;
+          if (et == 0) split_last = atomicAdd(a.split_cnt + seq.slot, 1) == seq.parts - 1;
           named_bar_sync(1, 128);
           if (!split_last) continue;
           __threadfence();
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             v[i] = sp == 0 ? __uint_as_float(r[i]) : v[i] + __uint_as_float(r[i]);
         }
         }
-        if (SPLIT || a.stage == 1) {
+        if (a.stage == 1) {
           // Gate (row 2j) and up (row 2j+1) sit in adjacent lanes. Even lanes
           // produce columns [0, half), odd lanes [half, kChunk): one shuffle
           // per column pair, no divergence.
@@ -725,15 +727,22 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
 }
 
 template <int BN>
-cudaError_t plan_bn(const MxArgs& a, int num_sms, GemmPlan* plan) {
+cudaError_t plan_bn(const MxArgs& a, int split, int num_sms, GemmPlan* plan) {
   using C = Cfg<BN>;
   static_assert(sizeof(MxArgs) <= sizeof(plan->args), "argument block");
-  // the tail-split kernel for stage 1 only where the tiles cannot fill
-  // kSplitMaxWaves waves even at the route count's upper bound (decode)
+  // By default the split-walk kernel only where it will split: the route
+  // count's upper bound gives fewer than kSplitMaxWaves waves of tiles
+  // (decode sizes). The split kernel walking whole tiles was measured 2-6 %
+  // slower per call than the plain one (backbone M=48 and 768), although the
+  // walk is the same; split = 1 takes it anyway (for routings whose bound is
+  // loose, e.g. an expert-parallel shard that drops most routes), 2 never.
+  // Stage 1 needs the split slots of the workspace.
   const void* fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, false>);
   if constexpr (BN <= 32) {
-    if (a.stage == 1 && a.split_part &&
-        static_cast<int64_t>(a.num_blocks) * a.n_tiles < kSplitMaxWaves * num_sms * C::kCtasPerSm)
+    const bool bound = static_cast<int64_t>(a.num_blocks) * a.n_tiles <
+                       static_cast<int64_t>(kSplitMaxWaves) * num_sms * C::kCtasPerSm;
+    const bool use = split == 1 || (split == 0 && bound);
+    if (use && (a.stage == 2 || a.split_part))
       fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, true>);
   }
   cudaError_t err = ensure_smem_attr(fn, C::kSmem);
@@ -741,7 +750,7 @@ cudaError_t plan_bn(const MxArgs& a, int num_sms, GemmPlan* plan) {
   const int tiles = a.num_blocks * a.n_tiles;
   const int slots = num_sms * C::kCtasPerSm;
   plan->kernel = fn;
-  // the split kernel spreads the tail tiles over every CTA slot
+  // the split kernel spreads the k-blocks over every CTA slot
   const bool split_kernel = fn != reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, false>);
   plan->grid = split_kernel || tiles > slots ? slots : tiles;
   plan->threads = kThreads;
@@ -804,11 +813,11 @@ cudaError_t prepare_gemm_mx(int stage, const GemmArgs& g, GemmPlan* plan) {
     return cudaErrorInvalidValue;
   const int sms = sm_count();
   switch (g.bm) {
-    case 16: return plan_bn<16>(a, sms, plan);
-    case 32: return plan_bn<32>(a, sms, plan);
-    case 64: return plan_bn<64>(a, sms, plan);
-    case 128: return plan_bn<128>(a, sms, plan);
-    case 256: return plan_bn<256>(a, sms, plan);
+    case 16: return plan_bn<16>(a, g.split, sms, plan);
+    case 32: return plan_bn<32>(a, g.split, sms, plan);
+    case 64: return plan_bn<64>(a, g.split, sms, plan);
+    case 128: return plan_bn<128>(a, g.split, sms, plan);
+    case 256: return plan_bn<256>(a, g.split, sms, plan);
   }
   return cudaErrorInvalidValue;
 }

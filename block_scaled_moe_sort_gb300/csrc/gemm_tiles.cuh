@@ -101,22 +101,24 @@ __device__ __forceinline__ int local_block_layout(const int32_t* ids, int R, int
   }
   for (int r = 4 * R4 + tid; r < R; r += nt) add(__ldg(ids + r));
   __syncthreads();
-  if (tid < 32) {   // exclusive scan of the padded block counts
-    int running = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int c = e < E ? cnt[e] : 0;
-      const int nb = (c + bn - 1) / bn;
-      int x = nb;
+  if (tid < 32) {   // exclusive scan of the block counts, in place
+    // lane l owns experts [l * per, (l + 1) * per): one warp scan of the lane sums
+    const int per = (E + 31) >> 5, e0 = lane * per, e1 = min(e0 + per, E);
+    int sum = 0;
+    for (int e = e0; e < e1; ++e) sum += (cnt[e] + bn - 1) / bn;
+    int x = sum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (e < E) cnt[e] = running + x - nb;
-      running += __shfl_sync(0xffffffffu, x, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
-    if (lane == 0) cnt[E] = running;
+    int run = x - sum;
+    for (int e = e0; e < e1; ++e) {
+      const int nb = (cnt[e] + bn - 1) / bn;
+      cnt[e] = run;
+      run += nb;
+    }
+    if (lane == 31) cnt[E] = x;
   }
   __syncthreads();
   const int nblk = cnt[E];
@@ -185,39 +187,48 @@ struct TileSeq {
 };
 
 
-// ------------------------------------------------------ stage-1 tail split
-// With few tiles (decode) the last, partial wave of stage-1 tiles leaves most
-// CTAs idle. SplitSeq walks stage-1 work units instead: with T tiles on a grid
-// of G CTAs, W = T / G whole waves and r = T - W * G tiles left over, the r
-// tiles are split into S = min(G / r, kblocks, kSplitMaxParts) K ranges when
-// W < kSplitMaxWaves. Units [0, W * G) are whole tiles; unit W * G + v is K
-// range v % S of tile W * G + v / S, whose partial sums go to slot v / S of
-// the split buffer (the range that finishes last runs the epilogue). Stage-1
+// ------------------------------------------------------------ split walk
+// With few tiles (decode) whole tiles leave CTAs idle in a partial last
+// wave. SplitSeq instead gives every CTA an equal, contiguous share of the
+// T * kblocks k-blocks of the T tiles (tiles route-block major, last route
+// block first) when T < kSplitMaxWaves * G for a grid of G CTAs: CTA c takes
+// k-blocks [c * L, (c + 1) * L) with L = ceil(T * kblocks / G), cut at tile
+// boundaries into units (tile, K range). A tile whose K range spans CTAs
+// f..l is computed in l - f + 1 parts. Stage 2 adds every part to the
+// accumulator like a whole tile (its epilogue is a sum); stage 1 adds the
+// parts into split slot f (at most one split tile starts in a CTA's range)
+// and the part that arrives last runs the epilogue from the slot. With more
+// tiles the CTAs walk whole tiles t = blockIdx.x + i * gridDim.x. Stage-1
 // tiles are route-block major, so the tiles that hold routes are the first
-// (P / bn) * n_tiles.
-constexpr int kSplitMaxWaves = 2;
-constexpr int kSplitMaxParts = 8;
+// (P / bn) * n_tiles in either stage's numbering here.
+constexpr int kSplitMaxWaves = 8;
 
 template <class Args, bool kExpert = true>
 struct SplitSeq {
-  int t, m_blk, n_tile, e, kb0, kb1, slot;
+  int m_blk, n_tile, e, kb0, kb1, slot, parts;   // the current unit
   bool valid;
-  int nt, nm, nn, ne, nkb0, nkb1, nslot;
+  int nm, nn, ne, nkb0, nkb1, nslot, nparts;     // the next one
   bool nvalid;
-  int wg, S, U, kblocks, pblk;
+  int pos, end;   // walk cursor: next k-block (split walk) or next tile, and the end
+  int kblocks, pblk, L;
+  bool split;
 
-  __device__ __forceinline__ bool locate(int u, int& m, int& n, int& k0, int& k1, int& sl,
-                                         const Args& a) const {
-    if (u >= U) return false;
+  __device__ __forceinline__ bool take(int& m, int& n, int& k0, int& k1, int& sl, int& np,
+                                       const Args& a) {
+    if (pos >= end) return false;
     int tt;
-    if (u < wg) {
-      tt = u; k0 = 0; k1 = kblocks; sl = -1;
+    if (split) {
+      tt = pos / kblocks;
+      k0 = pos - tt * kblocks;
+      k1 = min(kblocks, k0 + (end - pos));
+      pos += k1 - k0;
+      const int f = tt * kblocks / L, l = ((tt + 1) * kblocks - 1) / L;
+      np = l - f + 1;
+      sl = np > 1 ? f : -1;
     } else {
-      const int v = u - wg, part = v % S;
-      tt = wg + v / S;
-      k0 = part * kblocks / S;
-      k1 = (part + 1) * kblocks / S;
-      sl = v / S;
+      tt = pos;
+      pos += gridDim.x;
+      k0 = 0; k1 = kblocks; sl = -1; np = 1;
     }
     m = pblk - 1 - tt / a.n_tiles;   // last route block first
     n = tt % a.n_tiles;
@@ -228,23 +239,27 @@ struct SplitSeq {
     pblk = P / bn;
     const int T = pblk * a.n_tiles;
     const int G = gridDim.x;
-    const int W = T / G, r = T - W * G;
-    int parts = 1;
-    if (W < kSplitMaxWaves && r > 0 && r <= kSplitSlots) parts = min(min(G / r, kblocks), kSplitMaxParts);
-    if (parts > 1) { S = parts; wg = W * G; U = wg + r * parts; } else { S = 1; wg = T; U = T; }
-    t = blockIdx.x;
-    valid = locate(t, m_blk, n_tile, kb0, kb1, slot, a);
+    split = T > 0 && T < kSplitMaxWaves * G && G <= kSplitSlots;
+    if (split) {
+      const int N = T * kb;
+      L = (N + G - 1) / G;
+      pos = min(N, static_cast<int>(blockIdx.x) * L);
+      end = min(N, pos + L);
+    } else {
+      L = 1;
+      pos = blockIdx.x;
+      end = T;
+    }
+    valid = take(m_blk, n_tile, kb0, kb1, slot, parts, a);
     e = kExpert && valid ? expert_checked(a, __ldg(a.block_expert + m_blk)) : 0;
-    nt = t + gridDim.x;
-    nvalid = valid && locate(nt, nm, nn, nkb0, nkb1, nslot, a);
+    nvalid = valid && take(nm, nn, nkb0, nkb1, nslot, nparts, a);
     ne = kExpert && nvalid ? __ldg(a.block_expert + nm) : 0;   // checked in next()
   }
   __device__ __forceinline__ void next(const Args& a) {
-    t = nt; m_blk = nm; n_tile = nn; kb0 = nkb0; kb1 = nkb1; slot = nslot;
+    m_blk = nm; n_tile = nn; kb0 = nkb0; kb1 = nkb1; slot = nslot; parts = nparts;
     valid = nvalid;
     e = kExpert && valid ? expert_checked(a, ne) : 0;
-    nt = t + gridDim.x;
-    nvalid = valid && locate(nt, nm, nn, nkb0, nkb1, nslot, a);
+    nvalid = valid && take(nm, nn, nkb0, nkb1, nslot, nparts, a);
     ne = kExpert && nvalid ? __ldg(a.block_expert + nm) : 0;   // checked in next()
   }
 };

@@ -76,6 +76,7 @@ struct GemmArgs {
   bool a16;
   int M, H, Ip, E, topk, bm;
   int prefetch1, prefetch2;  // weight L2 prefetch lead per stage in k-blocks (0 = default)
+  int split;                 // split walk (a8w4): 0 = by the route bound, 1 = always, 2 = never
   int64_t p_max;
   const int32_t* topk_ids;   // the call's routing input (local layout at decode sizes)
   LocalGate gate;            // gated calls: router logits instead (topk_ids is then null)
@@ -92,7 +93,7 @@ struct GemmArgs {
   void* inter;          // [p_max, Ip]
   uint8_t* inter_sf;
   float* acc;           // [M, H]
-  float* split_part;    // stage-1 tail split: [kSplitSlots][block_m][128] FP32, zeroed per call
+  float* split_part;    // split walk, stage 1: [kSplitSlots][block_m][128] FP32, zeroed per call
   int32_t* split_cnt;   // [kSplitSlots], zeroed per call
   int32_t* status;
 };

@@ -136,11 +136,13 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
                             int H, int topk, const uint8_t* w1, const uint8_t* w1s,
                             const uint8_t* w2, const uint8_t* w2s, int E, int Ip, void* out,
                             void* ws, size_t ws_bytes, int bm_req, cudaStream_t s,
-                            const FrontGating* gate = nullptr, int pf1 = 0, int pf2 = 0) {
+                            const FrontGating* gate = nullptr, int pf1 = 0, int pf2 = 0,
+                            int split_walk = 0) {
   moe_status_t st = check_shape(M, H, Ip, E, topk);
   if (st != MOE_OK) return st;
   if (bm_req != 0 && !valid_bm(bm_req)) return MOE_ERR_UNSUPPORTED;
   if (pf1 < 0 || pf1 > kMaxPrefetch || pf2 < 0 || pf2 > kMaxPrefetch) return MOE_ERR_UNSUPPORTED;
+  if (split_walk < 0 || split_walk > 2 || (a16 && split_walk == 1)) return MOE_ERR_UNSUPPORTED;
   if (!ws || !w1 || !w1s || !w2 || !w2s) return MOE_ERR_INVALID_ARG;
   if (M > 0 && (!x || !ids || !wts || !out)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, ids, wts, w1, w1s, w2, w2s, out, ws};
@@ -205,6 +207,7 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   g.a16 = a16;
   g.M = M; g.H = H; g.Ip = Ip; g.E = E; g.topk = topk; g.bm = L.block_m;
   g.prefetch1 = pf1; g.prefetch2 = pf2;
+  g.split = split_walk;
   g.p_max = L.p_max;
   // the GEMMs may read topk_ids before their dependency wait only when it is
   // an input of the call (not when the gating kernel writes it)
@@ -417,11 +420,11 @@ moe_status_t fused_moe_a8w4_cfg(const void* x, const int32_t* topk_ids, const fl
                                 const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
                                 void* out, void* ws, size_t ws_bytes, const moe_call_config_t* cfg,
                                 moe_stream_t stream) {
-  if (cfg && cfg->reserved != 0) return MOE_ERR_INVALID_ARG;
   return fused_moe_impl(false, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
                         E, Ip, out, ws, ws_bytes, cfg ? cfg->block_m : 0,
                         reinterpret_cast<cudaStream_t>(stream), nullptr,
-                        cfg ? cfg->prefetch1 : 0, cfg ? cfg->prefetch2 : 0);
+                        cfg ? cfg->prefetch1 : 0, cfg ? cfg->prefetch2 : 0,
+                        cfg ? cfg->split : 0);
 }
 
 moe_status_t fused_moe_a16w4_cfg(const void* x, const int32_t* topk_ids, const float* topk_weights,
@@ -429,11 +432,11 @@ moe_status_t fused_moe_a16w4_cfg(const void* x, const int32_t* topk_ids, const f
                                  const uint8_t* w2, const uint8_t* w2_scale, int E, int Ip,
                                  void* out, void* ws, size_t ws_bytes, const moe_call_config_t* cfg,
                                  moe_stream_t stream) {
-  if (cfg && cfg->reserved != 0) return MOE_ERR_INVALID_ARG;
   return fused_moe_impl(true, x, topk_ids, topk_weights, M, H, topk, w1, w1_scale, w2, w2_scale,
                         E, Ip, out, ws, ws_bytes, cfg ? cfg->block_m : 0,
                         reinterpret_cast<cudaStream_t>(stream), nullptr,
-                        cfg ? cfg->prefetch1 : 0, cfg ? cfg->prefetch2 : 0);
+                        cfg ? cfg->prefetch1 : 0, cfg ? cfg->prefetch2 : 0,
+                        cfg ? cfg->split : 0);
 }
 
 moe_status_t fused_moe_a8w4(const void* x, const int32_t* topk_ids, const float* topk_weights,

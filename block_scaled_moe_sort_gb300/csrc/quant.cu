@@ -245,21 +245,24 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
     if (e >= 0) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
-  if (tid < 32) {   // exclusive scan of the padded counts
-    int running = 0;
-    for (int base = 0; base < a.E; base += 32) {
-      const int e = base + lane;
-      const int v = e < a.E ? (cnt[e] + a.bm - 1) / a.bm * a.bm : 0;
-      int xs = v;
+  if (tid < 32) {   // exclusive scan of the padded counts (block_m is a power of two)
+    // lane l owns experts [l * per, (l + 1) * per): one warp scan of the lane sums
+    const int per = (a.E + 31) >> 5, e0 = lane * per, e1 = min(e0 + per, a.E);
+    const int pad = a.bm - 1;
+    int sum = 0;
+    for (int e = e0; e < e1; ++e) sum += (cnt[e] + pad) & ~pad;
+    int xs = sum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, xs, o);
-        if (lane >= o) xs += y;
-      }
-      if (e < a.E) off[e] = running + xs - v;
-      running += __shfl_sync(0xffffffffu, xs, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, xs, o);
+      if (lane >= o) xs += y;
     }
-    if (lane == 0) off[a.E] = running;
+    int run = xs - sum;
+    for (int e = e0; e < e1; ++e) {
+      off[e] = run;
+      run += (cnt[e] + pad) & ~pad;
+    }
+    if (lane == 31) off[a.E] = xs;
   }
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) {
@@ -271,6 +274,9 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
   }
   __syncthreads();
   const int P = off[a.E];
+  // The layout out: the routes by CTA 0, the experts' segments and the tail
+  // over the whole grid (every CTA holds the layout), so no CTA carries much
+  // more than the others.
   if (blockIdx.x == 0) {
     if (tid == 0) {
       if (a.status) a.status[0] = 0;
@@ -285,20 +291,24 @@ __global__ void __launch_bounds__(256) front_tiny_kernel(const FrontArgs a) {
         a.sorted_w[p] = SLOTS > 0 ? w_s[r] : __ldg(a.wts + r);
       }
     }
-    for (int e = tid; e < a.E; e += blockDim.x) {
+  }
+  {
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+    const int64_t gs = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t e = g0; e < a.E; e += gs) {
       a.expert_off[e] = off[e];
       for (int p = off[e] + cnt[e]; p < off[e + 1]; ++p) {   // pads of the segment
         a.sorted_route[p] = R;
         a.sorted_w[p] = 0.f;
       }
-      for (int blk = off[e] / a.bm; blk < off[e + 1] / a.bm; ++blk) a.block_expert[blk] = e;
+      for (int blk = off[e] / a.bm; blk < off[e + 1] / a.bm; ++blk)
+        a.block_expert[blk] = static_cast<int32_t>(e);
     }
-    for (int64_t p = P + tid; p < a.p_max; p += blockDim.x) {   // tail
+    for (int64_t p = P + g0; p < a.p_max; p += gs) {   // tail
       a.sorted_route[p] = R;
       a.sorted_w[p] = 0.f;
     }
-    for (int64_t blk = P / a.bm + tid; blk < a.p_max / a.bm; blk += blockDim.x)
-      a.block_expert[blk] = -1;
+    for (int64_t blk = P / a.bm + g0; blk < a.p_max / a.bm; blk += gs) a.block_expert[blk] = -1;
   }
   // zero zero2, the stage-1 split buffers (grid-stride over all CTAs; the
   // accumulator is zeroed by the stage-1 GEMM after its tiles)

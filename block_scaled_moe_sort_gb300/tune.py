@@ -20,8 +20,11 @@ H, Ip, E, topk, a16, max_tokens, block_m, default_block_m, median_gain,
 wins, pairs, control_gain, control_wins, and the second knob, the weight L2
 prefetch leads: prefetch1, prefetch2 (0 = the library's defaults),
 prefetch_gain, prefetch_wins (``--knob prefetch`` measures them for the
-rows' block_m under the same gate). ``table_for`` turns the rows of one
-geometry into the ``block_m_table`` of ``MoeLayer``.
+rows' block_m under the same gate), and the third, the a8w4 GEMMs' split
+walk: split (0 = the library's rule, 1 = always, 2 = never), split_gain,
+split_wins (``--knob split``, the rows' block_m and leads fixed).
+``table_for`` turns the rows of one geometry into the ``block_m_table`` of
+``MoeLayer``.
 
   python -m block_scaled_moe_sort_gb300.tune --H 5120 --Ip 640 --E 384 --topk 6 \\
       --tokens 6 12 24 48 96 192 384 768 --buckets 8 16 32 64 128 256 512 1024 \\
@@ -49,11 +52,14 @@ MIN_GAIN = 0.01
 MIN_WIN_FRACTION = 25 / 31
 FIELDS = ["H", "Ip", "E", "topk", "a16", "max_tokens", "block_m", "default_block_m",
           "median_gain", "wins", "pairs", "control_gain", "control_wins",
-          "prefetch1", "prefetch2", "prefetch_gain", "prefetch_wins"]
+          "prefetch1", "prefetch2", "prefetch_gain", "prefetch_wins",
+          "split", "split_gain", "split_wins"]
 CANDIDATES = (16, 32, 64, 128)
 # (stage-1, stage-2) weight L2 prefetch leads tried against the defaults
 # (a8w4 4/2, a16w4 8/8), in 128-K weight tiles
 PREFETCH_CANDIDATES = ((8, 8), (24, 8), (32, 8), (16, 4), (16, 16), (4, 4))
+# the a8w4 GEMMs' split walk tried against the library's rule: always, never
+SPLIT_CANDIDATES = (1, 2)
 
 
 # ----------------------------------------------------------------- gate
@@ -75,8 +81,9 @@ def paired_gate(base: Sequence[float], cand: Sequence[float], min_gain: float = 
 
 # ---------------------------------------------------------------- table
 
-# fields a row may lack (tables written before the prefetch knob): 0
-_OPTIONAL = {"prefetch1": 0, "prefetch2": 0, "prefetch_gain": 0.0, "prefetch_wins": 0}
+# fields a row may lack (tables written before the prefetch or split knobs): 0
+_OPTIONAL = {"prefetch1": 0, "prefetch2": 0, "prefetch_gain": 0.0, "prefetch_wins": 0,
+             "split": 0, "split_gain": 0.0, "split_wins": 0}
 
 
 def write_table(rows: Iterable[dict], path: str) -> None:
@@ -91,14 +98,15 @@ def read_table(path: str) -> List[dict]:
     with open(path, newline="") as f:
         rows = list(csv.DictReader(f))
     ints = ["H", "Ip", "E", "topk", "a16", "max_tokens", "block_m", "default_block_m", "wins",
-            "pairs", "control_wins", "prefetch1", "prefetch2", "prefetch_wins"]
+            "pairs", "control_wins", "prefetch1", "prefetch2", "prefetch_wins", "split",
+            "split_wins"]
     for r in rows:
         for k, v in _OPTIONAL.items():
             if r.get(k) in (None, ""):
                 r[k] = v
         for k in ints:
             r[k] = int(r[k])
-        for k in ("median_gain", "control_gain", "prefetch_gain"):
+        for k in ("median_gain", "control_gain", "prefetch_gain", "split_gain"):
             r[k] = float(r[k])
     return rows
 
@@ -153,7 +161,7 @@ def random_inputs(M: int, H: int, E: int, topk: int, seed: int = 0, device: str 
 class _Graph:
     """One captured fused call with its own output and workspace."""
 
-    def __init__(self, layer, x, ids, w, block_m, stream, prefetch=(0, 0)):
+    def __init__(self, layer, x, ids, w, block_m, stream, prefetch=(0, 0), split=0):
         import torch
         M, k = ids.shape
         self.out = torch.empty(M, layer.H, dtype=torch.bfloat16, device=x.device)
@@ -162,11 +170,13 @@ class _Graph:
         self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
         with torch.cuda.stream(stream):
             for _ in range(2):
-                layer(x, ids, w, out=self.out, ws=self.ws, block_m=block_m, prefetch=prefetch)
+                layer(x, ids, w, out=self.out, ws=self.ws, block_m=block_m, prefetch=prefetch,
+                      split=split)
             torch.cuda.synchronize()
             self.g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(self.g, stream=stream):
-                layer(x, ids, w, out=self.out, ws=self.ws, block_m=block_m, prefetch=prefetch)
+                layer(x, ids, w, out=self.out, ws=self.ws, block_m=block_m, prefetch=prefetch,
+                      split=split)
         torch.cuda.synchronize()
 
     def measure(self, replays, flush, stream) -> float:
@@ -287,6 +297,49 @@ def tune_prefetch(rows: List[dict], candidates=PREFETCH_CANDIDATES, pairs: int =
     return out
 
 
+def tune_split(rows: List[dict], candidates=SPLIT_CANDIDATES, pairs: int = 31,
+               replays: int = 16, seed: int = 0, device: str = "cuda", log=print,
+               tokens: Optional[Sequence[int]] = None, E_route: Optional[int] = None,
+               shared: bool = False) -> List[dict]:
+    """Third knob (a8w4): for each row of one geometry (its block_m and
+    prefetch leads fixed), the GEMMs' split walk (1 = always, 2 = never)
+    against the library's rule, under the same gate. tokens[i] is the count
+    measured for rows[i] (default: its max_tokens)."""
+    import torch
+    if not rows:
+        return rows
+    r0 = rows[0]
+    H, Ip, E, topk, a16 = r0["H"], r0["Ip"], r0["E"], r0["topk"], bool(r0["a16"])
+    if a16:
+        raise ValueError("the split walk is an a8w4 knob")
+    tokens = list(tokens) if tokens else [r["max_tokens"] for r in rows]
+    layer = random_layer(H, Ip, E, a16, seed, device)
+    stream = torch.cuda.Stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    out = []
+    for r, M in zip(rows, tokens):
+        x, ids, w = random_inputs(M, H, E, topk, seed + M, device, E_route, shared)
+        bm, pf = r["block_m"], (r["prefetch1"], r["prefetch2"])
+        base = _Graph(layer, x, ids, w, bm, stream, prefetch=pf)
+        best = {"split": 0, "median_gain": 0.0, "wins": 0}
+        for sp in candidates:
+            cand = _Graph(layer, x, ids, w, bm, stream, prefetch=pf, split=sp)
+            tb, tc = _pairs(base, cand, pairs, replays, flush, stream)
+            gate = paired_gate(tb, tc)
+            log(f"M={M:6d} block_m {bm:3d} split rule vs {sp}: median gain "
+                f"{100 * gate['median_gain']:+6.2f}%  wins {gate['wins']}/{pairs}  "
+                f"{'ADOPT' if gate['accept'] else 'keep'}")
+            if gate["accept"] and gate["median_gain"] > best["median_gain"]:
+                best = {"split": sp, "median_gain": gate["median_gain"], "wins": gate["wins"]}
+            del cand
+        r = dict(r)
+        r["split"] = best["split"]
+        r["split_gain"] = round(best["median_gain"], 5)
+        r["split_wins"] = best["wins"]
+        out.append(r)
+    return out
+
+
 def main(argv: Optional[Sequence[str]] = None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--H", type=int, required=True)
@@ -305,26 +358,32 @@ def main(argv: Optional[Sequence[str]] = None) -> None:
                     help="experts the routing draws from (expert-parallel shard: the global count)")
     ap.add_argument("--shared", action="store_true",
                     help="the last routing column is the shared expert E-1 (weight 1)")
-    ap.add_argument("--knob", choices=["block_m", "prefetch"], default="block_m",
-                    help="prefetch: tune the weight prefetch leads of the geometry's rows "
-                         "in --table (their block_m fixed), measured at --tokens")
-    ap.add_argument("--table", default=PACKAGED_TABLE, help="rows the prefetch pass starts from")
+    ap.add_argument("--knob", choices=["block_m", "prefetch", "split"], default="block_m",
+                    help="prefetch / split: tune the weight prefetch leads / the split walk of "
+                         "the geometry's rows in --table (their other settings fixed), "
+                         "measured at --tokens")
+    ap.add_argument("--table", default=PACKAGED_TABLE,
+                    help="rows the prefetch and split passes start from")
     ap.add_argument("--pf-candidates", nargs="+", default=None,
                     help="prefetch pass: candidate leads as STAGE1,STAGE2 (e.g. 4,4 2,2)")
     ap.add_argument("--out", required=True)
     ap.add_argument("--append", action="store_true", help="keep the rows already in --out")
     a = ap.parse_args(argv)
-    if a.knob == "prefetch":
+    if a.knob in ("prefetch", "split"):
         mine = [r for r in read_table(a.table)
                 if (r["H"], r["Ip"], r["E"], r["topk"], r["a16"]) == (a.H, a.Ip, a.E, a.topk,
                                                                        int(a.a16))]
         mine.sort(key=lambda r: r["max_tokens"])
         if len(mine) != len(a.tokens):
             raise SystemExit(f"{len(mine)} rows of this geometry in --table, {len(a.tokens)} tokens")
+    if a.knob == "prefetch":
         cands = (tuple(tuple(int(v) for v in c.split(",")) for c in a.pf_candidates)
                  if a.pf_candidates else PREFETCH_CANDIDATES)
         rows = tune_prefetch(mine, candidates=cands, pairs=a.pairs, replays=a.replays,
                              tokens=a.tokens, E_route=a.E_route, shared=a.shared)
+    elif a.knob == "split":
+        rows = tune_split(mine, pairs=a.pairs, replays=a.replays, tokens=a.tokens,
+                          E_route=a.E_route, shared=a.shared)
     else:
         rows = tune_geometry(a.H, a.Ip, a.E, a.topk, a.a16, a.tokens, a.candidates, a.pairs,
                              a.replays, buckets=a.buckets, E_route=a.E_route, shared=a.shared)

@@ -112,14 +112,18 @@ def test_call_config_checks(L):
     args = [FAKE, FAKE, FAKE, 4, 256, 2, FAKE, FAKE, FAKE, FAKE, 8, 128, FAKE, FAKE, 1 << 40]
     for fn in ("fused_moe_a8w4_cfg", "fused_moe_a16w4_cfg"):
         f = getattr(L, fn)
-        bad = mm.MoeCallConfig(0, 0, 0, 1)                  # reserved must be 0
-        assert f(*args, ctypes.byref(bad), None) == 1
+        for sp in (-1, 3):                                  # split walk: 0, 1 or 2
+            bad = mm.MoeCallConfig(0, 0, 0, sp)
+            assert f(*args, ctypes.byref(bad), None) == 2
         far = mm.MoeCallConfig(0, 65, 0, 0)                 # lead past 64 tiles
         assert f(*args, ctypes.byref(far), None) == 2
         neg = mm.MoeCallConfig(0, 0, -1, 0)
         assert f(*args, ctypes.byref(neg), None) == 2
         odd = mm.MoeCallConfig(48, 0, 0, 0)                 # not a route block
         assert f(*args, ctypes.byref(odd), None) == 2
+    # a16w4 has no split walk: "always" is refused before any launch
+    on = mm.MoeCallConfig(0, 0, 0, 1)
+    assert L.fused_moe_a16w4_cfg(*args, ctypes.byref(on), None) == 2
 
 
 def test_device_status_decoding(L):

@@ -78,6 +78,20 @@ def test_explicit_prefetch_backbone(cuda_lib):
     print(compare(case, layer, False, tokens=sample_tokens(384, 8, 11)))
 
 
+@pytest.mark.parametrize("name,M,split", [("ep", 64, 1), ("backbone", 6, 2), ("draft", 40, 1)])
+def test_explicit_split_walk(cuda_lib, name, M, split):
+    # the third tuning knob (a8w4): the GEMMs' split walk forced on where the
+    # route count's bound is loose (the expert-parallel shard drops most
+    # routes; the draft bucket's second stage), and off where the rule would
+    # take it (both stages then walk whole tiles)
+    wts = __import__("moe_check").weights_for(name, 0)
+    layer = m.MoeLayer(wts["w1"], wts["w1_scale"], wts["w2"], wts["w2_scale"],
+                       block_m_table=[(1 << 30, 16, 0, 0, split)])
+    assert layer.split_for(M, 6) == split
+    case = mi.make_case(name, M, weights=wts)
+    print(compare(case, layer, False, tokens=None if M <= 6 else sample_tokens(M, 8, M)))
+
+
 def test_empty_experts_and_all_dropped_tokens(cuda_lib):
     shp = mi.small_shape(H=256, I=128, Ip=128, E=16, topk=2, E_route=64)
     w, layer = _small_layer(shp, 9)

@@ -110,17 +110,23 @@ def test_layer_lookup_by_topk_for_shipped_rows():
 def test_shipped_rows_by_geometry():
     from block_scaled_moe_sort_gb300 import shipped_block_m_rows
     draft = shipped_block_m_rows(5120, 640, 128, False)
-    # rows: (max_tokens, block_m[, prefetch1, prefetch2])
+    # rows: (max_tokens, block_m[, prefetch1, prefetch2[, split]])
     assert list(draft) == [3] and draft[3][-1][:2] == (1024, 32)
     backbone = shipped_block_m_rows(5120, 640, 384, False)
     assert [r[1] for r in backbone[6]] == [16] * 8
     # the measured prefetch leads: short ones won at every decode bucket
-    assert all(len(r) == 4 and 1 <= r[2] <= 8 and 1 <= r[3] <= 8 for r in backbone[6])
+    assert all(len(r) in (4, 5) and 1 <= r[2] <= 8 and 1 <= r[3] <= 8 for r in backbone[6])
+    # the split walk forced on where the route bound keeps the rule from it
+    # (buckets 16-128), never where the rule already takes it or it loses
+    split = lambda rows: {r[0]: (r[4] if len(r) == 5 else 0) for r in rows}
+    assert split(backbone[6]) == {8: 0, 16: 1, 32: 1, 64: 1, 128: 1, 256: 0, 512: 0, 1024: 0}
+    assert split(draft[3])[16] == 2 and split(draft[3])[64] == 1
     bm = lambda rows: {r[0]: r[1] for r in rows}
     # expert-parallel shard (96 local experts of 384, routing over all 384)
     ep = shipped_block_m_rows(5120, 2304, 96, False)
     assert list(ep) == [6] and ep[6][-1] == (16384, 128)          # prefill: defaults kept
     assert bm(ep[6])[32] == 32 and bm(ep[6])[2048] == 64
+    assert split(ep[6])[16] == 1 and split(ep[6])[4] == 0
     # a16w4: 384 top-6, and 385 top-7 with the shared expert as expert 384;
     # no prefetch lead passed the gate (the converters bound these calls)
     a16 = shipped_block_m_rows(5120, 768, 384, True)
@@ -151,3 +157,22 @@ def test_prefetch_knob_round_trip_and_lookup(tmp_path):
     assert MoeLayer.block_m_for(lay, 10) == 32 and MoeLayer.prefetch_for(lay, 10) == (0, 0)
     assert MoeLayer.block_m_for(lay, 500) == 64 and MoeLayer.prefetch_for(lay, 500) == (24, 4)
     assert MoeLayer.prefetch_for(lay, 5000) == (0, 0)
+
+
+def test_split_knob_round_trip_and_lookup(tmp_path):
+    # the third knob: split walk 0 (rule) / 1 (always) / 2 (never); a row
+    # that sets it carries the prefetch leads too (0 = defaults)
+    rows = [_row(64, 32), _row(1024, 64)]
+    rows[1].update(split=1, split_gain=0.04, split_wins=31)
+    p = tmp_path / "t.csv"
+    tune.write_table(rows, str(p))
+    back = tune.read_table(str(p))
+    assert (back[0]["split"], back[0]["split_gain"], back[0]["split_wins"]) == (0, 0.0, 0)
+    assert (back[1]["split"], back[1]["split_gain"], back[1]["split_wins"]) == (1, 0.04, 31)
+    lay = types.SimpleNamespace(block_m_table=[(64, 32), (1024, 64, 0, 0, 1), (4096, 64, 8, 2)])
+    assert MoeLayer.split_for(lay, 10) == 0 and MoeLayer.prefetch_for(lay, 10) == (0, 0)
+    assert MoeLayer.split_for(lay, 500) == 1 and MoeLayer.prefetch_for(lay, 500) == (0, 0)
+    assert MoeLayer.split_for(lay, 2000) == 0 and MoeLayer.prefetch_for(lay, 2000) == (8, 2)
+    assert MoeLayer.split_for(lay, 5000) == 0
+    with pytest.raises(ValueError):
+        tune.tune_split([dict(_row(64, 32), a16=1)])
