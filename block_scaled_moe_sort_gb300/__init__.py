@@ -364,8 +364,7 @@ def fused_moe_a16w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_pa
                     block_m: int = 0, prefetch=None, split: int = 0) -> torch.Tensor:
     """BF16-activation x MXFP4-weight fused MoE on weights prepacked by
     moe_prepack_weights_a16w4; returns BF16 [M, H]. block_m 0 = the
-    library's route block rule; prefetch as for fused_moe_a8w4; split 0 or 2
-    (there is no split walk in the a16w4 GEMMs)."""
+    library's route block rule; prefetch and split as for fused_moe_a8w4."""
     return _fused("fused_moe_a16w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
                   w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch, split)
 

@@ -85,6 +85,10 @@ struct Bf16Args {
   float* acc;                  // stage 2 out
   int prefetch;                // weight L2 prefetch lead in k-blocks
   int32_t* status;
+  // split walk, stage 1: FP32 partial sums [kSplitSlots][BN][128] and
+  // arrival counters [kSplitSlots], zero at the start of the call
+  float* split_part;
+  int32_t* split_cnt;
 };
 
 __host__ __device__ constexpr int pow2_cols(int c) {
@@ -130,14 +134,17 @@ struct Cfg16 {
                 "TMEM budget");
 };
 
-using Seq16 = TileSeq<Bf16Args>;          // producer: loads each tile's expert
-using Seq16R = TileSeq<Bf16Args, false>;  // other roles
-
-template <int BN>
+// SPLIT: the split walk (SplitSeq units; stage 1 finishes split tiles
+// through the partial-sum slots), else whole tiles (TileSeq)
+template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     moe_gemm_bf16w4_kernel(const __grid_constant__ CUtensorMap tmW,
                            const __grid_constant__ CUtensorMap tmX, const Bf16Args a) {
   using C = Cfg16<BN>;
+  // the producer's walk loads each tile's expert; the other roles' walks do not
+  using Seq16 = typename std::conditional<SPLIT, SplitSeq<Bf16Args>, TileSeq<Bf16Args>>::type;
+  using Seq16R = typename std::conditional<SPLIT, SplitSeq<Bf16Args, false>,
+                                           TileSeq<Bf16Args, false>>::type;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic so that the
   // compiler keeps every access below in the shared state space
@@ -151,6 +158,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
   __shared__ uint64_t drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ int split_last;
   __shared__ uint16_t s_blk_expert[kLocalMaxBlocks];   // local layout: expert of each route block
   __shared__ int s_nblk;                               // local layout: number of route blocks
 
@@ -228,29 +236,32 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           if (threadIdx.x == 0) MOE_TL(3 + a.stage, 1);
           P = *a.num_padded;
         }
-        cur.init(a, total_tiles, P, BN);
+        seq_init(cur, a, total_tiles, P, BN, kblocks);
         auto pf = cur;
-        int pf_kb = 0;
+        int pf_kb = seq_kb0(pf);
         auto pf_skip = [&]() {
-          if (++pf_kb == kblocks) {
-            pf_kb = 0;
-            pf.next(a, total_tiles, P, BN);
+          if (++pf_kb == seq_kb1(pf, kblocks)) {
+            seq_next(pf, a, total_tiles, P, BN);
+            if (pf.valid) pf_kb = seq_kb0(pf);
           }
         };
         auto pf_step = [&]() {
           if (!pf.valid) return;
           const int64_t tile =
               (static_cast<int64_t>(expert_of(pf)) * a.n_tiles + pf.n_tile) * kblocks + pf_kb;
-          // with the tile's weight scale atoms (512 B per k-block, contiguous)
-          if (pf_kb == 0) bulk_prefetch_l2(a.sfa + tile * 512, static_cast<uint32_t>(kblocks) * 512);
+          // with the unit's weight scale atoms (512 B per k-block, contiguous)
+          if (pf_kb == seq_kb0(pf))
+            bulk_prefetch_l2(a.sfa + tile * 512,
+                             static_cast<uint32_t>(seq_kb1(pf, kblocks) - pf_kb) * 512);
           bulk_prefetch_l2(a.w + tile * C::kRawBytes, C::kRawBytes);
           pf_skip();
         };
-        int kb = 0;
+        int kb = 0, kb_end = 0;
         int64_t tile0 = 0;
         auto set_tile = [&]() {
           tile0 = (static_cast<int64_t>(expert_of(cur)) * a.n_tiles + cur.n_tile) * kblocks;
-          kb = 0;
+          kb = seq_kb0(cur);
+          kb_end = seq_kb1(cur, kblocks);
         };
         auto arm = [&]() {
           mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
@@ -278,8 +289,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           if (prefetch) pf_step();
           else if (pf.valid) pf_skip();
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-          if (++kb == kblocks) {
-            cur.next(a, total_tiles, P, BN);
+          if (++kb == kb_end) {
+            seq_next(cur, a, total_tiles, P, BN);
             if (cur.valid) set_tile();
           }
         };
@@ -348,7 +359,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
       constexpr uint32_t idesc = idesc_dense(1, 1, kTileN, BN);
       const uint64_t b_desc0 = smem_desc(smem_u32(smem), 16, 1024, kSwizzle128B);
       Seq16R seq;
-      for (seq.init(a, total_tiles, P, BN); seq.valid && !abort_flag; seq.next(a, total_tiles, P, BN)) {
+      for (seq_init(seq, a, total_tiles, P, BN, kblocks); seq.valid && !abort_flag;
+           seq_next(seq, a, total_tiles, P, BN)) {
         const int ab = local % C::kAccBufs;
         const uint32_t acc_phase = (local / C::kAccBufs) & 1;
         ++local;
@@ -357,7 +369,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
         if (!ok0) { abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + C::kAccCol0 + ab * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const int kb_begin = seq_kb0(seq), kb_end = seq_kb1(seq, kblocks);
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           bool ok1, ok2;
           { WS_T0(); ok1 = mbar_wait(&full_bar[stage], phase, a.status); WS_ADD(1); }
           { WS_T0(); ok2 = ok1 && mbar_wait(&a_full[slot], slot_phase, a.status); WS_ADD(2); }
@@ -374,7 +387,7 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
             // A: 8 TMEM columns (16 BF16) per MMA
             const int h = kk / (kAtomK / kMmaK), off = (kk % (kAtomK / kMmaK)) * 2;
             mma_f16_tmem_a(d_tmem, a_tmem + kk * (kMmaK / 2),
-                           bd + h * (C::kBAtomBytes >> 4) + off, idesc, (kb | kk) != 0);
+                           bd + h * (C::kBAtomBytes >> 4) + off, idesc, kb > kb_begin || kk != 0);
           }
           tc_commit(&empty_bar[stage]);         // frees the smem stage and the TMEM slot
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -404,9 +417,10 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     uint32_t lag_phase = 0;
     int done = 0;                 // k-blocks converted so far
     Seq16R seq;
-    for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
+    for (seq_init(seq, a, total_tiles, P, BN, kblocks); seq.valid;
+         seq_next(seq, a, total_tiles, P, BN)) {
       bool stop = false;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = seq_kb0(seq); kb < seq_kb1(seq, kblocks); ++kb) {
         bool okc1 = !abort_flag, okc2;
 #ifdef MOE_WAIT_STATS
         const bool rep = threadIdx.x == 192;
@@ -490,7 +504,8 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
     const int R = a.M * a.topk;
     int local = 0;
     Seq16R seq;
-    for (seq.init(a, total_tiles, P, BN); seq.valid; seq.next(a, total_tiles, P, BN)) {
+    for (seq_init(seq, a, total_tiles, P, BN, kblocks); seq.valid;
+         seq_next(seq, a, total_tiles, P, BN)) {
       const int m_blk = seq.m_blk, n_tile = seq.n_tile;
       const int ab = local % C::kAccBufs;
       const uint32_t acc_phase = (local / C::kAccBufs) & 1;
@@ -520,21 +535,53 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           tmem + C::kAccCol0 + ab * BN + (static_cast<uint32_t>(quad * 32) << 16);
       const int64_t p_base = static_cast<int64_t>(m_blk) * BN;
       constexpr int kChunk = BN < 32 ? BN : 32;
+      auto load_acc = [&](int c0, float (&v)[32]) {
+        uint32_t r32[32];
+        if constexpr (kChunk == 32) {
+          tmem_ld_32x32b_x32(d_tmem + c0, r32);
+        } else {
+          uint32_t r16[16];
+          tmem_ld_32x32b_x16(d_tmem + c0, r16);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r32[i] = r16[i];
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r32[i]);
+      };
+      // Split walk, stage 1: a part of a split tile adds its partial sums to
+      // the tile's slot (feature row fastest: a warp adds 128 contiguous
+      // bytes), releases the accumulator and counts itself in; the part that
+      // arrives last reads the complete sums back from L2 and runs the
+      // epilogue. (Stage 2 adds every part to the accumulator directly.)
+      float* part = nullptr;
+      if constexpr (SPLIT) {
+        if (seq.slot >= 0 && a.stage == 1) {
+          part = a.split_part + static_cast<int64_t>(seq.slot) * BN * 128;
+          for (int c0 = 0; c0 < BN; c0 += kChunk) {
+            float v[32];
+            load_acc(c0, v);
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) atomicAdd(part + (c0 + i) * 128 + row, v[i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ab]);
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (et == 0) split_last = atomicAdd(a.split_cnt + seq.slot, 1) == seq.parts - 1;
+          named_bar_sync(1, 128);
+          if (!split_last) continue;
+          __threadfence();
+        }
+      }
       for (int c0 = 0; c0 < BN; c0 += kChunk) {
         float v[32];
-        {
-          uint32_t r32[32];
-          if constexpr (kChunk == 32) {
-            tmem_ld_32x32b_x32(d_tmem + c0, r32);
-          } else {
-            uint32_t r16[16];
-            tmem_ld_32x32b_x16(d_tmem + c0, r16);
+        if (part) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r32[i] = r16[i];
-          }
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < kChunk; ++i) v[i] = __uint_as_float(r32[i]);
+          for (int i = 0; i < kChunk; ++i) v[i] = __ldcg(part + (c0 + i) * 128 + row);
+        } else {
+          load_acc(c0, v);
         }
         if (a.stage == 1) {
           // gate/up pairs in adjacent lanes; even lanes take columns [0, half)
@@ -614,9 +661,11 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      if (!part) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      }
     }
     if (threadIdx.x == 64) MOE_TL(3 + a.stage, 5);
     if (a.stage == 1) {
@@ -669,16 +718,26 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
 }
 
 template <int BN>
-cudaError_t plan_bn(const Bf16Args& a, int num_sms, GemmPlan* plan) {
+cudaError_t plan_bn(const Bf16Args& a, int split, int num_sms, GemmPlan* plan) {
   using C = Cfg16<BN>;
   static_assert(sizeof(Bf16Args) <= sizeof(plan->args), "argument block");
-  const void* fn = reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN>);
-  cudaError_t err = ensure_smem_attr(fn, C::kSmem);
-  if (err != cudaSuccess) return err;
   const int tiles = a.num_blocks * a.n_tiles;
   const int slots = num_sms * C::kCtasPerSm;
+  // The split-walk kernel as for a8w4: by default only where the route
+  // count's upper bound gives fewer than kSplitMaxWaves waves of tiles;
+  // split = 1 always, 2 never. Stage 1 needs the split slots.
+  const void* fn = reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN, false>);
+  if constexpr (BN <= 32) {
+    const bool bound = static_cast<int64_t>(tiles) < static_cast<int64_t>(kSplitMaxWaves) * slots;
+    const bool use = split == 1 || (split == 0 && bound);
+    if (use && (a.stage == 2 || a.split_part))
+      fn = reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN, true>);
+  }
+  cudaError_t err = ensure_smem_attr(fn, C::kSmem);
+  if (err != cudaSuccess) return err;
   plan->kernel = fn;
-  plan->grid = tiles < slots ? tiles : slots;
+  const bool split_kernel = fn != reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN, false>);
+  plan->grid = split_kernel || tiles > slots ? slots : tiles;
   plan->threads = C::kThreads;
   plan->smem = C::kSmem;
   memcpy(plan->args, &a, sizeof(a));
@@ -710,6 +769,8 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   a.prefetch = stage == 1 ? (g.prefetch1 > 0 ? g.prefetch1 : 8)
                          : (g.prefetch2 > 0 ? g.prefetch2 : 8);
   a.status = g.status;
+  a.split_part = g.split_part;
+  a.split_cnt = g.split_cnt;
   plan->grid = 0;
   if (a.num_blocks == 0) return cudaSuccess;
   const void* xb = stage == 1 ? g.act : g.inter;
@@ -727,11 +788,11 @@ cudaError_t prepare_gemm_bf16w4(int stage, const GemmArgs& g, GemmPlan* plan) {
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   switch (g.bm) {
-    case 16: return plan_bn<16>(a, sms, plan);
-    case 32: return plan_bn<32>(a, sms, plan);
-    case 64: return plan_bn<64>(a, sms, plan);
-    case 128: return plan_bn<128>(a, sms, plan);
-    case 256: return plan_bn<256>(a, sms, plan);
+    case 16: return plan_bn<16>(a, g.split, sms, plan);
+    case 32: return plan_bn<32>(a, g.split, sms, plan);
+    case 64: return plan_bn<64>(a, g.split, sms, plan);
+    case 128: return plan_bn<128>(a, g.split, sms, plan);
+    case 256: return plan_bn<256>(a, g.split, sms, plan);
   }
   return cudaErrorInvalidValue;
 }

@@ -93,8 +93,8 @@ void build_layout(int M, int H, int Ip, int E, int topk, bool a16, int bm_req,
   L->inter_off = take(pm * Ip * (a16 ? 2 : 1));
   L->inter_sf_off = take(a16 ? 0 : nblk * (Ip / 128) * atoms * 512);
   L->acc_off = take(static_cast<int64_t>(M) * H * 4);
-  // stage-1 tail split buffers (a8w4 decode block sizes only)
-  const bool split = !a16 && bm <= 32;
+  // split-walk slots of stage 1 (decode block sizes)
+  const bool split = bm <= 32;
   L->split_part_off = take(split ? static_cast<int64_t>(kSplitSlots) * bm * 128 * 4 : 0);
   L->split_cnt_off = take(split ? kSplitSlots * 4 : 0);
   L->total_bytes = o;
@@ -142,7 +142,7 @@ moe_status_t fused_moe_impl(bool a16, const void* x, const int32_t* ids, const f
   if (st != MOE_OK) return st;
   if (bm_req != 0 && !valid_bm(bm_req)) return MOE_ERR_UNSUPPORTED;
   if (pf1 < 0 || pf1 > kMaxPrefetch || pf2 < 0 || pf2 > kMaxPrefetch) return MOE_ERR_UNSUPPORTED;
-  if (split_walk < 0 || split_walk > 2 || (a16 && split_walk == 1)) return MOE_ERR_UNSUPPORTED;
+  if (split_walk < 0 || split_walk > 2) return MOE_ERR_UNSUPPORTED;
   if (!ws || !w1 || !w1s || !w2 || !w2s) return MOE_ERR_INVALID_ARG;
   if (M > 0 && (!x || !ids || !wts || !out)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, ids, wts, w1, w1s, w2, w2s, out, ws};

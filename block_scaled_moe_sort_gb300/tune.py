@@ -20,7 +20,7 @@ H, Ip, E, topk, a16, max_tokens, block_m, default_block_m, median_gain,
 wins, pairs, control_gain, control_wins, and the second knob, the weight L2
 prefetch leads: prefetch1, prefetch2 (0 = the library's defaults),
 prefetch_gain, prefetch_wins (``--knob prefetch`` measures them for the
-rows' block_m under the same gate), and the third, the a8w4 GEMMs' split
+rows' block_m under the same gate), and the third, the GEMMs' split
 walk: split (0 = the library's rule, 1 = always, 2 = never), split_gain,
 split_wins (``--knob split``, the rows' block_m and leads fixed).
 ``table_for`` turns the rows of one geometry into the ``block_m_table`` of
@@ -58,7 +58,7 @@ CANDIDATES = (16, 32, 64, 128)
 # (stage-1, stage-2) weight L2 prefetch leads tried against the defaults
 # (a8w4 4/2, a16w4 8/8), in 128-K weight tiles
 PREFETCH_CANDIDATES = ((8, 8), (24, 8), (32, 8), (16, 4), (16, 16), (4, 4))
-# the a8w4 GEMMs' split walk tried against the library's rule: always, never
+# the GEMMs' split walk tried against the library's rule: always, never
 SPLIT_CANDIDATES = (1, 2)
 
 
@@ -301,17 +301,15 @@ def tune_split(rows: List[dict], candidates=SPLIT_CANDIDATES, pairs: int = 31,
                replays: int = 16, seed: int = 0, device: str = "cuda", log=print,
                tokens: Optional[Sequence[int]] = None, E_route: Optional[int] = None,
                shared: bool = False) -> List[dict]:
-    """Third knob (a8w4): for each row of one geometry (its block_m and
-    prefetch leads fixed), the GEMMs' split walk (1 = always, 2 = never)
-    against the library's rule, under the same gate. tokens[i] is the count
-    measured for rows[i] (default: its max_tokens)."""
+    """Third knob: for each row of one geometry (its block_m and prefetch
+    leads fixed), the GEMMs' split walk (1 = always, 2 = never) against the
+    library's rule, under the same gate. tokens[i] is the count measured for
+    rows[i] (default: its max_tokens)."""
     import torch
     if not rows:
         return rows
     r0 = rows[0]
     H, Ip, E, topk, a16 = r0["H"], r0["Ip"], r0["E"], r0["topk"], bool(r0["a16"])
-    if a16:
-        raise ValueError("the split walk is an a8w4 knob")
     tokens = list(tokens) if tokens else [r["max_tokens"] for r in rows]
     layer = random_layer(H, Ip, E, a16, seed, device)
     stream = torch.cuda.Stream()

@@ -191,7 +191,7 @@ moe_status_t moe_prepack_scales_mx(const uint8_t* scale, int E, int N, int K, ui
  * later call with the same or a smaller shape. Contents need no
  * initialisation. Two calls in flight on different streams need different
  * workspaces. Results are not bitwise reproducible from call to call: the
- * routing-weighted sum (and, for small a8w4 calls, the parts of the tiles
+ * routing-weighted sum (and, for small calls, the parts of the tiles
  * that the split walk spreads over several CTAs) is added in FP32 by atomic
  * reductions whose order varies; the sorted lists are deterministic, and so
  * is the intermediate outside the split stage-1 tiles.
@@ -286,13 +286,12 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
  *   prefetch1  stage-1 weight L2 prefetch lead in 128-K weight tiles, 1..64
  *              (default a8w4 4, a16w4 8)
  *   prefetch2  the same for stage 2 (default a8w4 2, a16w4 8)
- *   split      a8w4 at block_m <= 32: the GEMMs' split walk, in which every
- *              CTA takes an equal share of the tiles' K blocks (a tile spread
+ *   split      at block_m <= 32: the GEMMs' split walk, in which every CTA
+ *              takes an equal share of the tiles' K blocks (a tile spread
  *              over several CTAs is computed in parts) when there are fewer
  *              than 8 waves of tiles. 0 = where the route count's upper bound
  *              gives fewer than 8 waves, 1 = always (the grid decides per call
- *              from the real tile count), 2 = never. a16w4 has no split walk:
- *              0 or 2 there.
+ *              from the real tile count), 2 = never.
  * Out-of-range values give MOE_ERR_UNSUPPORTED. cfg NULL = all defaults.
  * The result does not depend on the prefetch leads (they only move weight
  * tiles into L2 earlier or later); the split walk changes the order of FP32

@@ -121,9 +121,6 @@ def test_call_config_checks(L):
         assert f(*args, ctypes.byref(neg), None) == 2
         odd = mm.MoeCallConfig(48, 0, 0, 0)                 # not a route block
         assert f(*args, ctypes.byref(odd), None) == 2
-    # a16w4 has no split walk: "always" is refused before any launch
-    on = mm.MoeCallConfig(0, 0, 0, 1)
-    assert L.fused_moe_a16w4_cfg(*args, ctypes.byref(on), None) == 2
 
 
 def test_device_status_decoding(L):

@@ -128,10 +128,12 @@ def test_shipped_rows_by_geometry():
     assert bm(ep[6])[32] == 32 and bm(ep[6])[2048] == 64
     assert split(ep[6])[16] == 1 and split(ep[6])[4] == 0
     # a16w4: 384 top-6, and 385 top-7 with the shared expert as expert 384;
-    # no prefetch lead passed the gate (the converters bound these calls)
+    # no prefetch lead passed the gate (the converters bound these calls),
+    # the split walk forced on did at the decode buckets (up to 1536)
     a16 = shipped_block_m_rows(5120, 768, 384, True)
     assert list(a16) == [6] and bm(a16[6])[1024] == 32 and bm(a16[6])[4096] == 128
-    assert all(len(r) == 2 for r in a16[6])
+    assert all(len(r) == 2 or r[2:] == (0, 0, 1) for r in a16[6])
+    assert split(a16[6]) == {12: 1, 256: 1, 1024: 1, 1536: 1, 4096: 0, 16384: 0}
     assert list(shipped_block_m_rows(5120, 768, 385, True)) == [7]
     assert shipped_block_m_rows(4096, 640, 384, False) == {}     # not tuned
     lay = types.SimpleNamespace(block_m_table=[], _bm_by_topk=draft)
@@ -174,5 +176,3 @@ def test_split_knob_round_trip_and_lookup(tmp_path):
     assert MoeLayer.split_for(lay, 500) == 1 and MoeLayer.prefetch_for(lay, 500) == (0, 0)
     assert MoeLayer.split_for(lay, 2000) == 0 and MoeLayer.prefetch_for(lay, 2000) == (8, 2)
     assert MoeLayer.split_for(lay, 5000) == 0
-    with pytest.raises(ValueError):
-        tune.tune_split([dict(_row(64, 32), a16=1)])
