@@ -71,7 +71,7 @@ struct Bf16Args {
   int N, K;
   int n_tiles;
   int num_blocks;
-  int n_group_log2;            // stage 2: log2 of the feature tiles per walk group
+  int n_group_log2;            // stage 2: log2 of the feature tiles per walk group (-1: route-block major)
   int local;                   // derive the route layout from topk_ids (decode sizes)
   const int32_t* topk_ids;
   LocalGate gate;        // gated calls: the routing input is the router logits

@@ -69,7 +69,7 @@ struct MxArgs {
   int N, K;              // weight rows per expert / reduction length
   int n_tiles;           // N / 128
   int num_blocks;        // p_max / block_m
-  int n_group_log2;      // stage 2: log2 of the feature tiles per walk group
+  int n_group_log2;      // stage 2: log2 of the feature tiles per walk group (-1: route-block major)
   int local;             // derive the route layout from topk_ids (decode sizes)
   const int32_t* topk_ids;
   LocalGate gate;        // gated calls: the routing input is the router logits

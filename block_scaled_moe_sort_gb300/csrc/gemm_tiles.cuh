@@ -1,9 +1,10 @@
 // Tile walk shared by the grouped GEMM kernels: a tile is (route block,
 // weight-row tile); stage 1 walks route-block major (the n-tiles of a block
-// reuse its activation rows), stage 2 in groups of 2^n_group_log2 feature tiles,
-// route-block major inside a group (the FP32 reductions of concurrently
-// running tiles stay in the group's slice of the accumulator, i.e. in L2,
-// and the intermediate is read once per group).
+// reuse its activation rows), and so does stage 2 at decode sizes
+// (n_group_log2 < 0); larger stage-2 walks go in groups of 2^n_group_log2
+// feature tiles, route-block major inside a group (the FP32 reductions of
+// concurrently running tiles stay in the group's slice of the accumulator,
+// i.e. in L2, and the intermediate is read once per group).
 #pragma once
 #include <cstdint>
 #include "common.cuh"
@@ -131,7 +132,7 @@ __device__ __forceinline__ int local_block_layout(const int32_t* ids, int R, int
 
 template <class Args>
 __device__ __forceinline__ void tile_coords(int t, const Args& a, int& m_blk, int& n_tile) {
-  if (a.stage == 1) {
+  if (a.stage == 1 || a.n_group_log2 < 0) {
     m_blk = t / a.n_tiles;
     n_tile = t % a.n_tiles;
   } else {
