@@ -353,8 +353,8 @@ def fused_moe_a8w4(x, topk_ids, topk_weights, w1_packed, w1_scale_packed, w2_pac
     """FP8-activation x MXFP4-weight fused MoE on prepacked weights; returns
     BF16 [M, H]. block_m 0 = the library's route block rule; prefetch
     (stage-1, stage-2 weight L2 prefetch lead in weight tiles, 0 = default)
-    and split (the GEMMs' split walk: 0 = the library's rule, 1 = always,
-    2 = never) go through fused_moe_a8w4_cfg."""
+    and split (the GEMMs' split walk: 0 = the library's choice, 1 = the
+    walk, 2 = whole tiles only) go through fused_moe_a8w4_cfg."""
     return _fused("fused_moe_a8w4", x, topk_ids, topk_weights, w1_packed, w1_scale_packed,
                   w2_packed, w2_scale_packed, E, Ip, out, ws, stream, block_m, prefetch, split)
 
@@ -595,7 +595,7 @@ class MoeLayer:
         return (int(row[2]), int(row[3])) if row and len(row) >= 4 else (0, 0)
 
     def split_for(self, M: int, topk: Optional[int] = None) -> int:
-        """Split walk for an M-token call (0 = the library's rule)."""
+        """Split walk for an M-token call (0 = the library's choice)."""
         row = MoeLayer._row_for(self, M, topk)
         return int(row[4]) if row and len(row) >= 5 else 0
 

@@ -575,14 +575,11 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
           __threadfence();
         }
       }
-      for (int c0 = 0; c0 < BN; c0 += kChunk) {
-        float v[32];
-        if (part) {
-#pragma unroll
-          for (int i = 0; i < kChunk; ++i) v[i] = __ldcg(part + (c0 + i) * 128 + row);
-        } else {
-          load_acc(c0, v);
-        }
+      // The chunk's epilogue once its FP32 values are in v (from TMEM, or
+      // from the split slot for the last part of a split stage-1 tile); two
+      // loops keep the TMEM path free of the slot pointer (with it in one
+      // loop the a8w4 split kernel's stage 2 ran 2x slower).
+      auto finish = [&](const int c0, float (&v)[32]) {
         if (a.stage == 1) {
           // gate/up pairs in adjacent lanes; even lanes take columns [0, half)
           constexpr int half = kChunk / 2;
@@ -660,6 +657,20 @@ __global__ void __launch_bounds__(Cfg16<BN>::kThreads, Cfg16<BN>::kCtasPerSm)
               if (tk[j] >= 0) atomicAdd(col + static_cast<int64_t>(tk[j]) * a.H, v[4 * q + j] * wk[j]);
           }
         }
+      };
+      if (SPLIT && part) {
+        for (int c0 = 0; c0 < BN; c0 += kChunk) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < kChunk; ++i) v[i] = __ldcg(part + (c0 + i) * 128 + row);
+          finish(c0, v);
+        }
+      } else {
+        for (int c0 = 0; c0 < BN; c0 += kChunk) {
+          float v[32];
+          load_acc(c0, v);
+          finish(c0, v);
+        }
       }
       if (!part) {
         tc_fence_before();
@@ -723,14 +734,11 @@ cudaError_t plan_bn(const Bf16Args& a, int split, int num_sms, GemmPlan* plan) {
   static_assert(sizeof(Bf16Args) <= sizeof(plan->args), "argument block");
   const int tiles = a.num_blocks * a.n_tiles;
   const int slots = num_sms * C::kCtasPerSm;
-  // The split-walk kernel as for a8w4: by default only where the route
-  // count's upper bound gives fewer than kSplitMaxWaves waves of tiles;
-  // split = 1 always, 2 never. Stage 1 needs the split slots.
+  // The split-walk kernel as for a8w4: at route blocks <= 32 unless the
+  // call asks for whole tiles (split = 2). Stage 1 needs the split slots.
   const void* fn = reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN, false>);
   if constexpr (BN <= 32) {
-    const bool bound = static_cast<int64_t>(tiles) < static_cast<int64_t>(kSplitMaxWaves) * slots;
-    const bool use = split == 1 || (split == 0 && bound);
-    if (use && (a.stage == 2 || a.split_part))
+    if (split != 2 && (a.stage == 2 || a.split_part))
       fn = reinterpret_cast<const void*>(&moe_gemm_bf16w4_kernel<BN, true>);
   }
   cudaError_t err = ensure_smem_attr(fn, C::kSmem);

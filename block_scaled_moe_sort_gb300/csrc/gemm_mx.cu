@@ -514,34 +514,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
           __threadfence();
         }
       }
-      for (int c0 = 0; c0 < BN; c0 += kChunk) {
-        float v[32];
-        bool from_part = false;
-        if constexpr (SPLIT) {
-          if (part) {
-#pragma unroll
-            for (int i = 0; i < kChunk; ++i) v[i] = __ldcg(part + (c0 + i) * 128 + row);
-            from_part = true;
-          }
-        }
-        if (!from_part) {
-#pragma unroll
-        for (int sp = 0; sp < C::kSplit; ++sp) {
-          uint32_t r[32];
-          if constexpr (kChunk == 32) {
-            tmem_ld_32x32b_x32(d_tmem + sp * BN + c0, r);
-          } else {
-            uint32_t r16[16];
-            tmem_ld_32x32b_x16(d_tmem + sp * BN + c0, r16);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = r16[i];
-          }
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < kChunk; ++i)
-            v[i] = sp == 0 ? __uint_as_float(r[i]) : v[i] + __uint_as_float(r[i]);
-        }
-        }
+      // The chunk's epilogue once its FP32 values are in v (from TMEM, or
+      // from the split slot for the last part of a split stage-1 tile). The
+      // two loops below keep the TMEM path free of the slot pointer: with
+      // it in one loop the split kernel's stage 2 ran 2x slower.
+      auto finish = [&](const int c0, float (&v)[32]) {
         if (a.stage == 1) {
           // Gate (row 2j) and up (row 2j+1) sit in adjacent lanes. Even lanes
           // produce columns [0, half), odd lanes [half, kChunk): one shuffle
@@ -644,6 +621,35 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
               if (tk[j] >= 0) atomicAdd(col + static_cast<int64_t>(tk[j]) * a.H, v[4 * q + j] * wk[j]);
           }
         }
+      };
+      if (SPLIT && part) {
+        for (int c0 = 0; c0 < BN; c0 += kChunk) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < kChunk; ++i) v[i] = __ldcg(part + (c0 + i) * 128 + row);
+          finish(c0, v);
+        }
+      } else {
+        for (int c0 = 0; c0 < BN; c0 += kChunk) {
+          float v[32];
+#pragma unroll
+          for (int sp = 0; sp < C::kSplit; ++sp) {
+            uint32_t r[32];
+            if constexpr (kChunk == 32) {
+              tmem_ld_32x32b_x32(d_tmem + sp * BN + c0, r);
+            } else {
+              uint32_t r16[16];
+              tmem_ld_32x32b_x16(d_tmem + sp * BN + c0, r16);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) r[i] = r16[i];
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i)
+              v[i] = sp == 0 ? __uint_as_float(r[i]) : v[i] + __uint_as_float(r[i]);
+          }
+          finish(c0, v);
+        }
       }
       if (!SPLIT || !part) {
         tc_fence_before();
@@ -730,19 +736,15 @@ template <int BN>
 cudaError_t plan_bn(const MxArgs& a, int split, int num_sms, GemmPlan* plan) {
   using C = Cfg<BN>;
   static_assert(sizeof(MxArgs) <= sizeof(plan->args), "argument block");
-  // By default the split-walk kernel only where it will split: the route
-  // count's upper bound gives fewer than kSplitMaxWaves waves of tiles
-  // (decode sizes). The split kernel walking whole tiles was measured 2-6 %
-  // slower per call than the plain one (backbone M=48 and 768), although the
-  // walk is the same; split = 1 takes it anyway (for routings whose bound is
-  // loose, e.g. an expert-parallel shard that drops most routes), 2 never.
+  // The split-walk kernel at route blocks <= 32 unless the call asks for
+  // whole tiles (split = 2): it splits where the real tiles are fewer than
+  // kSplitMaxWaves waves and otherwise walks whole tiles route-block major,
+  // measured as fast as the plain kernel or faster at every decode size but
+  // the draft geometry's 10-20 tokens (up to 5 % faster at 192-768 tokens).
   // Stage 1 needs the split slots of the workspace.
   const void* fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, false>);
   if constexpr (BN <= 32) {
-    const bool bound = static_cast<int64_t>(a.num_blocks) * a.n_tiles <
-                       static_cast<int64_t>(kSplitMaxWaves) * num_sms * C::kCtasPerSm;
-    const bool use = split == 1 || (split == 0 && bound);
-    if (use && (a.stage == 2 || a.split_part))
+    if (split != 2 && (a.stage == 2 || a.split_part))
       fn = reinterpret_cast<const void*>(&moe_gemm_mx_kernel<BN, true>);
   }
   cudaError_t err = ensure_smem_attr(fn, C::kSmem);

@@ -21,8 +21,9 @@ wins, pairs, control_gain, control_wins, and the second knob, the weight L2
 prefetch leads: prefetch1, prefetch2 (0 = the library's defaults),
 prefetch_gain, prefetch_wins (``--knob prefetch`` measures them for the
 rows' block_m under the same gate), and the third, the GEMMs' split
-walk: split (0 = the library's rule, 1 = always, 2 = never), split_gain,
-split_wins (``--knob split``, the rows' block_m and leads fixed).
+walk: split (0 = the library's choice, 1 = the split walk, 2 = whole
+tiles only), split_gain, split_wins (``--knob split``, the rows' block_m
+and leads fixed).
 ``table_for`` turns the rows of one geometry into the ``block_m_table`` of
 ``MoeLayer``.
 
@@ -58,7 +59,7 @@ CANDIDATES = (16, 32, 64, 128)
 # (stage-1, stage-2) weight L2 prefetch leads tried against the defaults
 # (a8w4 4/2, a16w4 8/8), in 128-K weight tiles
 PREFETCH_CANDIDATES = ((8, 8), (24, 8), (32, 8), (16, 4), (16, 16), (4, 4))
-# the GEMMs' split walk tried against the library's rule: always, never
+# the GEMMs' split walk tried against the library's choice: the walk, whole tiles
 SPLIT_CANDIDATES = (1, 2)
 
 
@@ -302,8 +303,8 @@ def tune_split(rows: List[dict], candidates=SPLIT_CANDIDATES, pairs: int = 31,
                tokens: Optional[Sequence[int]] = None, E_route: Optional[int] = None,
                shared: bool = False) -> List[dict]:
     """Third knob: for each row of one geometry (its block_m and prefetch
-    leads fixed), the GEMMs' split walk (1 = always, 2 = never) against the
-    library's rule, under the same gate. tokens[i] is the count measured for
+    leads fixed), the GEMMs' split walk (1 = the walk, 2 = whole tiles only)
+    against the library's choice, under the same gate. tokens[i] is the count measured for
     rows[i] (default: its max_tokens)."""
     import torch
     if not rows:
@@ -324,7 +325,7 @@ def tune_split(rows: List[dict], candidates=SPLIT_CANDIDATES, pairs: int = 31,
             cand = _Graph(layer, x, ids, w, bm, stream, prefetch=pf, split=sp)
             tb, tc = _pairs(base, cand, pairs, replays, flush, stream)
             gate = paired_gate(tb, tc)
-            log(f"M={M:6d} block_m {bm:3d} split rule vs {sp}: median gain "
+            log(f"M={M:6d} block_m {bm:3d} split default vs {sp}: median gain "
                 f"{100 * gate['median_gain']:+6.2f}%  wins {gate['wins']}/{pairs}  "
                 f"{'ADOPT' if gate['accept'] else 'keep'}")
             if gate["accept"] and gate["median_gain"] > best["median_gain"]:
@@ -364,6 +365,8 @@ def main(argv: Optional[Sequence[str]] = None) -> None:
                     help="rows the prefetch and split passes start from")
     ap.add_argument("--pf-candidates", nargs="+", default=None,
                     help="prefetch pass: candidate leads as STAGE1,STAGE2 (e.g. 4,4 2,2)")
+    ap.add_argument("--split-candidates", type=int, nargs="+", default=list(SPLIT_CANDIDATES),
+                    help="split pass: split values tried against the library's choice")
     ap.add_argument("--out", required=True)
     ap.add_argument("--append", action="store_true", help="keep the rows already in --out")
     a = ap.parse_args(argv)
@@ -380,8 +383,8 @@ def main(argv: Optional[Sequence[str]] = None) -> None:
         rows = tune_prefetch(mine, candidates=cands, pairs=a.pairs, replays=a.replays,
                              tokens=a.tokens, E_route=a.E_route, shared=a.shared)
     elif a.knob == "split":
-        rows = tune_split(mine, pairs=a.pairs, replays=a.replays, tokens=a.tokens,
-                          E_route=a.E_route, shared=a.shared)
+        rows = tune_split(mine, candidates=tuple(a.split_candidates), pairs=a.pairs,
+                          replays=a.replays, tokens=a.tokens, E_route=a.E_route, shared=a.shared)
     else:
         rows = tune_geometry(a.H, a.Ip, a.E, a.topk, a.a16, a.tokens, a.candidates, a.pairs,
                              a.replays, buckets=a.buckets, E_route=a.E_route, shared=a.shared)

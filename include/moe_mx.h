@@ -289,9 +289,9 @@ moe_status_t fused_moe_a16w4_bm(const void* x, const int32_t* topk_ids, const fl
  *   split      at block_m <= 32: the GEMMs' split walk, in which every CTA
  *              takes an equal share of the tiles' K blocks (a tile spread
  *              over several CTAs is computed in parts) when there are fewer
- *              than 8 waves of tiles. 0 = where the route count's upper bound
- *              gives fewer than 8 waves, 1 = always (the grid decides per call
- *              from the real tile count), 2 = never.
+ *              than 8 waves of tiles, and whole tiles otherwise. 0 = the
+ *              library's choice (the split walk), 1 = the split walk,
+ *              2 = whole tiles only.
  * Out-of-range values give MOE_ERR_UNSUPPORTED. cfg NULL = all defaults.
  * The result does not depend on the prefetch leads (they only move weight
  * tiles into L2 earlier or later); the split walk changes the order of FP32

@@ -80,10 +80,10 @@ def test_explicit_prefetch_backbone(cuda_lib):
 
 @pytest.mark.parametrize("name,M,split", [("ep", 64, 1), ("backbone", 6, 2), ("draft", 40, 1)])
 def test_explicit_split_walk(cuda_lib, name, M, split):
-    # the third tuning knob (a8w4): the GEMMs' split walk forced on where the
-    # route count's bound is loose (the expert-parallel shard drops most
-    # routes; the draft bucket's second stage), and off where the rule would
-    # take it (both stages then walk whole tiles)
+    # the third tuning knob: the GEMMs' split walk asked for explicitly (the
+    # expert-parallel shard, whose routes are mostly dropped; the draft at 40
+    # tokens) and switched off (the plain kernels, whole tiles in both
+    # stages, where the library would split)
     wts = __import__("moe_check").weights_for(name, 0)
     layer = m.MoeLayer(wts["w1"], wts["w1_scale"], wts["w2"], wts["w2_scale"],
                        block_m_table=[(1 << 30, 16, 0, 0, split)])

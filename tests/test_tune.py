@@ -116,24 +116,23 @@ def test_shipped_rows_by_geometry():
     assert [r[1] for r in backbone[6]] == [16] * 8
     # the measured prefetch leads: short ones won at every decode bucket
     assert all(len(r) in (4, 5) and 1 <= r[2] <= 8 and 1 <= r[3] <= 8 for r in backbone[6])
-    # the split walk forced on where the route bound keeps the rule from it
-    # (buckets 16-128), never where the rule already takes it or it loses
+    # the split walk is the library's choice; whole tiles only won at one
+    # draft bucket (16)
     split = lambda rows: {r[0]: (r[4] if len(r) == 5 else 0) for r in rows}
-    assert split(backbone[6]) == {8: 0, 16: 1, 32: 1, 64: 1, 128: 1, 256: 0, 512: 0, 1024: 0}
-    assert split(draft[3])[16] == 2 and split(draft[3])[64] == 1
+    assert set(split(backbone[6]).values()) == {0}
+    assert split(draft[3]) == {8: 0, 16: 2, 32: 0, 64: 0, 128: 0, 256: 0, 512: 0, 1024: 0}
     bm = lambda rows: {r[0]: r[1] for r in rows}
     # expert-parallel shard (96 local experts of 384, routing over all 384)
     ep = shipped_block_m_rows(5120, 2304, 96, False)
     assert list(ep) == [6] and ep[6][-1] == (16384, 128)          # prefill: defaults kept
     assert bm(ep[6])[32] == 32 and bm(ep[6])[2048] == 64
-    assert split(ep[6])[16] == 1 and split(ep[6])[4] == 0
+    assert set(split(ep[6]).values()) == {0}
     # a16w4: 384 top-6, and 385 top-7 with the shared expert as expert 384;
-    # no prefetch lead passed the gate (the converters bound these calls),
-    # the split walk forced on did at the decode buckets (up to 1536)
+    # no prefetch lead and no split setting passed the gate (the converters
+    # bound these calls)
     a16 = shipped_block_m_rows(5120, 768, 384, True)
     assert list(a16) == [6] and bm(a16[6])[1024] == 32 and bm(a16[6])[4096] == 128
-    assert all(len(r) == 2 or r[2:] == (0, 0, 1) for r in a16[6])
-    assert split(a16[6]) == {12: 1, 256: 1, 1024: 1, 1536: 1, 4096: 0, 16384: 0}
+    assert all(len(r) == 2 for r in a16[6])
     assert list(shipped_block_m_rows(5120, 768, 385, True)) == [7]
     assert shipped_block_m_rows(4096, 640, 384, False) == {}     # not tuned
     lay = types.SimpleNamespace(block_m_table=[], _bm_by_topk=draft)
