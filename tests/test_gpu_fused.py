@@ -78,18 +78,21 @@ def test_explicit_prefetch_backbone(cuda_lib):
     print(compare(case, layer, False, tokens=sample_tokens(384, 8, 11)))
 
 
-@pytest.mark.parametrize("name,M,split", [("ep", 64, 1), ("backbone", 6, 2), ("draft", 40, 1)])
+@pytest.mark.parametrize("name,M,split", [("ep", 64, 1), ("backbone", 6, 2), ("draft", 40, 1),
+                                          ("a16w4_384", 12, 2), ("a16w4_385", 300, 2),
+                                          ("a16w4_385", 300, 1)])
 def test_explicit_split_walk(cuda_lib, name, M, split):
     # the third tuning knob: the GEMMs' split walk asked for explicitly (the
     # expert-parallel shard, whose routes are mostly dropped; the draft at 40
     # tokens) and switched off (the plain kernels, whole tiles in both
-    # stages, where the library would split)
+    # stages, where the library would split), on both variants
+    a16 = mi.SHAPES[name].a16
     wts = __import__("moe_check").weights_for(name, 0)
-    layer = m.MoeLayer(wts["w1"], wts["w1_scale"], wts["w2"], wts["w2_scale"],
+    layer = m.MoeLayer(wts["w1"], wts["w1_scale"], wts["w2"], wts["w2_scale"], a16=a16,
                        block_m_table=[(1 << 30, 16, 0, 0, split)])
     assert layer.split_for(M, 6) == split
     case = mi.make_case(name, M, weights=wts)
-    print(compare(case, layer, False, tokens=None if M <= 6 else sample_tokens(M, 8, M)))
+    print(compare(case, layer, a16, tokens=None if M <= 12 else sample_tokens(M, 8, M)))
 
 
 def test_empty_experts_and_all_dropped_tokens(cuda_lib):
