@@ -277,11 +277,11 @@ def tune_prefetch(rows: List[dict], candidates=PREFETCH_CANDIDATES, pairs: int =
     out = []
     for r, M in zip(rows, tokens):
         x, ids, w = random_inputs(M, H, E, topk, seed + M, device, E_route, shared)
-        bm = r["block_m"]
-        base = _Graph(layer, x, ids, w, bm, stream)
+        bm, sp = r["block_m"], r.get("split", 0)   # the row's split walk stays as it is
+        base = _Graph(layer, x, ids, w, bm, stream, split=sp)
         best = {"prefetch": (0, 0), "median_gain": 0.0, "wins": 0}
         for pf in candidates:
-            cand = _Graph(layer, x, ids, w, bm, stream, prefetch=pf)
+            cand = _Graph(layer, x, ids, w, bm, stream, prefetch=pf, split=sp)
             tb, tc = _pairs(base, cand, pairs, replays, flush, stream)
             gate = paired_gate(tb, tc)
             log(f"M={M:6d} block_m {bm:3d} prefetch default vs {pf}: median gain "
