@@ -114,8 +114,11 @@ def test_shipped_rows_by_geometry():
     assert list(draft) == [3] and draft[3][-1][:2] == (1024, 32)
     backbone = shipped_block_m_rows(5120, 640, 384, False)
     assert [r[1] for r in backbone[6]] == [16] * 8
-    # the measured prefetch leads: short ones won at every decode bucket
-    assert all(len(r) in (4, 5) and 1 <= r[2] <= 8 and 1 <= r[3] <= 8 for r in backbone[6])
+    # the weight prefetch leads: against the short defaults (4 / 2) only the
+    # bucket 16 row passed the gate (2 / 2)
+    pf = lambda rows: {r[0]: (tuple(r[2:4]) if len(r) >= 4 else (0, 0)) for r in rows}
+    assert pf(backbone[6])[16] == (2, 2)
+    assert set(pf(backbone[6]).values()) == {(0, 0), (2, 2)}
     # the split walk is the library's choice; whole tiles only won at one
     # draft bucket (16)
     split = lambda rows: {r[0]: (r[4] if len(r) == 5 else 0) for r in rows}
