@@ -140,7 +140,8 @@ def test_shipped_rows_by_geometry():
     assert shipped_block_m_rows(4096, 640, 384, False) == {}     # not tuned
     lay = types.SimpleNamespace(block_m_table=[], _bm_by_topk=draft)
     assert MoeLayer.block_m_for(lay, 640, 3) == 32 and MoeLayer.block_m_for(lay, 320, 3) == 16
-    assert MoeLayer.prefetch_for(lay, 640, 3) == draft[3][-1][2:]
+    assert MoeLayer.prefetch_for(lay, 640, 3) == pf(draft[3])[1024] == (0, 0)
+    assert MoeLayer.split_for(lay, 10, 3) == 2 and MoeLayer.split_for(lay, 640, 3) == 0
 
 
 def test_prefetch_knob_round_trip_and_lookup(tmp_path):
