@@ -10,7 +10,8 @@ namespace moe {
 constexpr int kMaxExperts = 512;   // expert ids fit 9 bits (route sort)
 constexpr int kMaxTopk = 16;
 constexpr int kMaxPrefetch = 64;   // weight L2 prefetch lead per call, k-blocks
-// Split-buffer tiles of the stage-1 tail split (>= the GEMM grid: SMs x 2).
+// Stage-1 slots of the split walk (>= the GEMM grid: SMs x 2; a split tile
+// takes the slot of the first CTA whose share it starts in).
 constexpr int kSplitSlots = 320;
 // Up to this many routes the call's front (sort + gather) is one launch.
 constexpr int kFrontMaxRoutes = 256;

@@ -85,7 +85,7 @@ struct MxArgs {
   float* acc;            // stage 2 out: [M, H]
   int prefetch;          // weight L2 prefetch lead in k-blocks
   int32_t* status;
-  // stage-1 tail split (decode): FP32 partial sums [kSplitSlots][BN][128] and
+  // split walk, stage 1: FP32 partial sums [kSplitSlots][BN][128] and
   // arrival counters [kSplitSlots], zero at the start of the call
   float* split_part;
   int32_t* split_cnt;

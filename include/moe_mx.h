@@ -213,7 +213,7 @@ typedef struct {
   int64_t inter_off;     /* a8w4: E4M3 [p_max, Ip]; a16w4: BF16 [p_max, Ip] */
   int64_t inter_sf_off;  /* a8w4: scale atoms [p_max/block_m][Ip/128][ceil(block_m/128)][512] */
   int64_t acc_off;       /* float [M, H] routing-weighted sum before BF16 rounding */
-  int64_t split_part_off;   /* a8w4, block_m <= 32: float [320][block_m][128] partial sums of
+  int64_t split_part_off;   /* block_m <= 32: float [320][block_m][128] partial sums of
                                stage-1 tiles whose K range is split across CTAs; else empty */
   int64_t split_cnt_off;    /* int32 [320] arrival counters of those tiles; else empty */
   int64_t total_bytes;
